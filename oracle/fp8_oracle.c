@@ -1,0 +1,286 @@
+/*
+ * CPU oracle for the FP8_DYNAMIC W8A8 linear layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file: only tests/, __graft_entry__.smoke() and bench.py's CPU
+ * baseline and reference arm use it.  It shares no code, header, table or
+ * constant generator with the CUDA library.
+ *
+ * It is deliberately plain and slow: one value at a time, in the order the
+ * pages describe, with fp64 wherever a step has no fixed precision.
+ *
+ * Sources (page title, section):
+ *   [P2] "FP8 Inference Explained, in depth", sections "The numbers in one
+ *        byte" (E4M3 layout, the round_e4m3 semantics, the fake_quant worked
+ *        row), "Scales and their granularity" (x_fp8 = round(x / s),
+ *        s = amax / 448) and "Inside a quantized linear layer" (per-token x
+ *        per-channel scales move outside the K sum; FP32 accumulation).
+ *   [P3] "FP8 Quantization", sections "FP8 Representation" (bias 7,
+ *        96.0 = 0 1101 100) and "How FP8 Matmul Works at the Hardware Level"
+ *        (FP8 x FP8 -> FP32 accumulate -> BF16 out).
+ *   [P4] "Quantization: FP8 inference and KV-cache quantization", section
+ *        "Dynamic scales or static scales" (per-token scale amax/448,
+ *        saturating conversion).
+ *
+ * Readings taken where the pages leave a step open:
+ *   - the activation scale is s = fl32(amax / 448) and each value is divided
+ *     by s in IEEE fp32 (round to nearest even) before the E4M3 rounding;
+ *   - an all-zero row gets s = 1;
+ *   - conversion saturates at +-448 (never NaN) and keeps the sign of zero;
+ *   - the GEMM result is kept in fp64 (not rounded to BF16).
+ *
+ * Build: gcc -O2 -std=c11 -fopenmp -ffp-contract=off -fPIC -shared.
+ * No -ffast-math: every fp32 division below must be IEEE.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define E4M3_MAX 448.0
+
+/* ------------------------------------------------------------------------ */
+/* E4M3 (float8_e4m3fn) codec                                               */
+/* ------------------------------------------------------------------------ */
+
+/* Value of one E4M3 code.  [P2 "The numbers in one byte"], [P3 "FP8
+ * Representation"]: bit 7 sign, bits 6..3 exponent field E with bias 7,
+ * bits 2..0 mantissa m.  E = 0 is subnormal with value m * 2^-9; otherwise
+ * (1 + m/8) * 2^(E-7).  The fn variant has no infinities: only E = 15,
+ * m = 7 is NaN, so the largest finite value is (1 + 6/8) * 2^8 = 448. */
+double orc_e4m3_decode(uint8_t c)
+{
+    int sign = (c >> 7) & 1;
+    int E = (c >> 3) & 15;
+    int m = c & 7;
+    double v;
+    if (E == 15 && m == 7)
+        return NAN;
+    if (E == 0)
+        v = ldexp((double)m, -9);
+    else
+        v = ldexp(1.0 + m / 8.0, E - 7);
+    return sign ? -v : v;
+}
+
+/* Round-half-to-even of a non-negative double that is exactly representable
+ * (the caller divides by a power of two, so no rounding has happened yet). */
+static double round_half_even(double t)
+{
+    double f = floor(t);
+    double d = t - f;
+    if (d > 0.5)
+        return f + 1.0;
+    if (d < 0.5)
+        return f;
+    return (fmod(f, 2.0) == 0.0) ? f : f + 1.0;
+}
+
+/* The pages' round_e4m3 semantics [P2 "The numbers in one byte"]:
+ *   zero and NaN pass through; otherwise keep the sign, clamp |x| to 448,
+ *   take the binade exponent e = max(floor(log2 |x|), -6) (-6 is the
+ *   smallest normal exponent, so below 2^-6 the step stays 2^-9), quantize
+ *   with step 2^(e-3) (three mantissa bits) rounding half to even, and clamp
+ *   to 448 again.
+ * floor(log2 a) is taken from frexp, which is exact, instead of a floating
+ * point log2. */
+double orc_round_e4m3(double x)
+{
+    double a, step, q;
+    int ex, e;
+    if (x == 0.0 || isnan(x))
+        return x;
+    a = fabs(x);
+    if (a > E4M3_MAX)
+        a = E4M3_MAX;
+    frexp(a, &ex);            /* a = f * 2^ex with f in [0.5, 1) */
+    e = ex - 1;               /* floor(log2 a) */
+    if (e < -6)
+        e = -6;
+    step = ldexp(1.0, e - 3);
+    q = round_half_even(a / step) * step;
+    if (q > E4M3_MAX)
+        q = E4M3_MAX;
+    return copysign(q, x);
+}
+
+/* Bit pattern of a value that is already on the E4M3 grid (the output of
+ * orc_round_e4m3).  Inverse of orc_e4m3_decode by the same field layout. */
+uint8_t orc_e4m3_pack(double v)
+{
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs(v);
+    int ex, e, E, m;
+    if (isnan(v))
+        return 0x7F;
+    if (a == 0.0)
+        return sign;
+    frexp(a, &ex);
+    e = ex - 1;
+    if (e < -6) {                         /* subnormal: a = m * 2^-9 */
+        m = (int)ldexp(a, 9);
+        return (uint8_t)(sign | m);
+    }
+    E = e + 7;
+    m = (int)((ldexp(a, -e) - 1.0) * 8.0);
+    return (uint8_t)(sign | (E << 3) | m);
+}
+
+/* Saturating, round-to-nearest-even conversion of a real value to E4M3. */
+uint8_t orc_e4m3_encode(double x)
+{
+    if (isnan(x))
+        return 0x7F;
+    return orc_e4m3_pack(orc_round_e4m3(x));
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dynamic per-token (and per-output-channel) quantization                  */
+/* ------------------------------------------------------------------------ */
+
+/* bfloat16 is the top half of an IEEE binary32, so widening is exact. */
+static float bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+float orc_bf16_to_f32(uint16_t b) { return bf16_to_f32(b); }
+
+/* Quantize one row of fp32 values with its own dynamic scale.
+ * [P2 "Scales and their granularity"]: s = amax / 448 and x_fp8 = round(x/s);
+ * [P4 "Dynamic scales or static scales"]: one scale per token, computed on
+ * every forward pass, so the row maximum lands exactly on 448.
+ * Both the scale and every quotient are IEEE fp32 divisions. */
+static void quant_row_f32(const float* x, int64_t K, uint8_t* q, float* s_out)
+{
+    float amax = 0.0f, s;
+    int64_t k;
+    for (k = 0; k < K; ++k) {
+        float a = fabsf(x[k]);
+        if (a > amax)
+            amax = a;
+    }
+    s = (amax > 0.0f) ? amax / 448.0f : 1.0f;
+    for (k = 0; k < K; ++k) {
+        volatile float t = x[k] / s;   /* force an fp32 quotient */
+        q[k] = orc_e4m3_encode((double)t);
+    }
+    *s_out = s;
+}
+
+/* Rows of bf16 bit patterns (activations [M,K] or weights [N,K]).  The row
+ * is widened to fp32 (exact) value by value and read twice: once for amax,
+ * once for the quotients. */
+void orc_quant_rows_bf16(const uint16_t* x, int64_t R, int64_t K, int64_t ldx,
+                         uint8_t* q, int64_t ldq, float* s)
+{
+    int64_t r;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (r = 0; r < R; ++r) {
+        const uint16_t* xr = x + r * ldx;
+        uint8_t* qr = q + r * ldq;
+        float amax = 0.0f, sc;
+        int64_t k;
+        for (k = 0; k < K; ++k) {
+            float a = fabsf(bf16_to_f32(xr[k]));
+            if (a > amax)
+                amax = a;
+        }
+        sc = (amax > 0.0f) ? amax / 448.0f : 1.0f;
+        for (k = 0; k < K; ++k) {
+            volatile float t = bf16_to_f32(xr[k]) / sc;   /* fp32 quotient */
+            qr[k] = orc_e4m3_encode((double)t);
+        }
+        s[r] = sc;
+    }
+}
+
+/* Rows of fp32 values: used to check the pages' fp32 worked examples. */
+void orc_quant_rows_f32(const float* x, int64_t R, int64_t K, int64_t ldx,
+                        uint8_t* q, int64_t ldq, float* s)
+{
+    int64_t r;
+    for (r = 0; r < R; ++r)
+        quant_row_f32(x + r * ldx, K, q + r * ldq, s + r);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Scaled FP8 GEMM + dequant epilogue                                       */
+/* ------------------------------------------------------------------------ */
+
+/* Every finite E4M3 value times 2^9 is an integer of magnitude at most
+ * 448 * 512 = 229376 < 2^18, so a product of two scaled codes is an exact
+ * integer below 2^36 and a K-term sum stays below 2^51 for K < 2^15: the
+ * dot product of the codes is computed exactly in int64. */
+static int64_t code_times_512(uint8_t c)
+{
+    return (int64_t)ldexp(orc_e4m3_decode(c), 9);
+}
+
+/* acc[m,n] = sum_k (512 q_x[m,k]) * (512 q_w[n,k])  (exact, int64).
+ * q_x is [M,K] row-major, q_w is [N,K] row-major (nn.Linear layout). */
+void orc_gemm_exact(const uint8_t* qx, int64_t ldqx, const uint8_t* qw, int64_t ldqw,
+                    int64_t M, int64_t N, int64_t K, int64_t* acc)
+{
+    int64_t tab[256];
+    int64_t m;
+    int i;
+    for (i = 0; i < 256; ++i)
+        tab[i] = ((i & 0x7F) == 0x7F) ? 0 : code_times_512((uint8_t)i);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (m = 0; m < M; ++m) {
+        int64_t n, k;
+        for (n = 0; n < N; ++n) {
+            int64_t sum = 0;
+            for (k = 0; k < K; ++k)
+                sum += tab[qx[m * ldqx + k]] * tab[qw[n * ldqw + k]];
+            acc[m * N + n] = sum;
+        }
+    }
+}
+
+/* [P2 "Inside a quantized linear layer"]: both scales are constant along k,
+ * so y[m,n] = s_tok[m] * s_w[n] * (q_x[m,:] . q_w[n,:]).  Kept in fp64. */
+void orc_epilogue(const int64_t* acc, int64_t M, int64_t N,
+                  const float* s_tok, const float* s_w, double* y)
+{
+    int64_t m, n;
+    for (m = 0; m < M; ++m)
+        for (n = 0; n < N; ++n)
+            y[m * N + n] = ldexp((double)acc[m * N + n], -18)
+                           * (double)s_tok[m] * (double)s_w[n];
+}
+
+/* The same result at a list of (row, col) points only, for shapes whose full
+ * output is too large to compute on the CPU. */
+void orc_linear_points(const uint8_t* qx, int64_t ldqx, const float* s_tok,
+                       const uint8_t* qw, int64_t ldqw, const float* s_w, int64_t K,
+                       int64_t npts, const int64_t* rows, const int64_t* cols, double* y)
+{
+    int64_t tab[256];
+    int64_t p;
+    int i;
+    for (i = 0; i < 256; ++i)
+        tab[i] = ((i & 0x7F) == 0x7F) ? 0 : code_times_512((uint8_t)i);
+#pragma omp parallel for schedule(static)
+    for (p = 0; p < npts; ++p) {
+        int64_t m = rows[p], n = cols[p], k, sum = 0;
+        for (k = 0; k < K; ++k)
+            sum += tab[qx[m * ldqx + k]] * tab[qw[n * ldqw + k]];
+        y[p] = ldexp((double)sum, -18) * (double)s_tok[m] * (double)s_w[n];
+    }
+}
+
+int orc_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
