@@ -1,0 +1,183 @@
+"""ctypes binding of the C ABI in include/fp8w8a8.h.
+
+Argument marshalling only: every step of the layer runs in the CUDA library
+(``_build/libfp8w8a8.so``).  If the library is missing the calls raise; there
+is no CPU or PyTorch fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY_PATH = os.path.join(_HERE, "_build", "libfp8w8a8.so")
+
+FP8_OK = 0
+STATUS_NAMES = {
+    0: "FP8_OK",
+    1: "FP8_ERR_INVALID_ARG",
+    2: "FP8_ERR_UNSUPPORTED",
+    3: "FP8_ERR_WORKSPACE",
+    4: "FP8_ERR_CUDA",
+    5: "FP8_ERR_TIMEOUT",
+}
+
+_lock = threading.Lock()
+_lib = None
+
+_i64 = ctypes.c_int64
+_vp = ctypes.c_void_p
+_st = ctypes.c_int
+
+
+class Fp8Error(RuntimeError):
+    """A call of the library returned a status other than FP8_OK."""
+
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library, with argument types declared."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIBRARY_PATH):
+            raise RuntimeError(
+                f"CUDA library not built ({LIBRARY_PATH}); run "
+                "`python -m fp8_w8a8_quantized_gb300.build` (needs nvcc)")
+        L = ctypes.CDLL(LIBRARY_PATH)
+        L.fp8_quant_per_token.restype = _st
+        L.fp8_quant_per_token.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp]
+        L.fp8_quant_per_channel_weights.restype = _st
+        L.fp8_quant_per_channel_weights.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp]
+        L.fp8_scaled_gemm.restype = _st
+        L.fp8_scaled_gemm.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp,
+                                      ctypes.c_size_t, _vp]
+        L.fp8_linear.restype = _st
+        L.fp8_linear.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, ctypes.c_size_t, _vp]
+        L.fp8_linear_workspace_size.restype = ctypes.c_size_t
+        L.fp8_linear_workspace_size.argtypes = [_i64, _i64, _i64]
+        L.fp8_scaled_gemm_workspace_size.restype = ctypes.c_size_t
+        L.fp8_scaled_gemm_workspace_size.argtypes = [_i64, _i64, _i64]
+        L.fp8_status_string.restype = ctypes.c_char_p
+        L.fp8_status_string.argtypes = [_st]
+        L.fp8_device_status.restype = _st
+        L.fp8_device_status.argtypes = [ctypes.c_int]
+        _lib = L
+        return L
+
+
+def _check(status: int, what: str):
+    if status != FP8_OK:
+        raise Fp8Error(status, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def _rows(t: torch.Tensor, name: str):
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+        raise ValueError(f"{name} must be 2-D with unit stride along K")
+    return t.shape[0], t.shape[1], t.stride(0)
+
+
+def fp8_status_string(status: int) -> str:
+    return lib().fp8_status_string(status).decode()
+
+
+def fp8_device_status(clear: bool = False) -> int:
+    """FP8_OK, or FP8_ERR_TIMEOUT if a kernel gave up a bounded wait."""
+    return lib().fp8_device_status(1 if clear else 0)
+
+
+def fp8_linear_workspace_size(M: int, N: int, K: int) -> int:
+    return int(lib().fp8_linear_workspace_size(M, N, K))
+
+
+def fp8_quant_per_token(x: torch.Tensor, xq: torch.Tensor | None = None,
+                        s_tok: torch.Tensor | None = None, stream=None):
+    """bf16 [M, K] -> (E4M3 codes uint8 [M, K], fp32 scales [M])."""
+    M, K, ldx = _rows(x, "x")
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if s_tok is None:
+        s_tok = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _check(lib().fp8_quant_per_token(_ptr(x), M, K, ldx, _ptr(xq), xq.stride(0) if M else K,
+                                     _ptr(s_tok), _stream(stream)), "fp8_quant_per_token")
+    return xq, s_tok
+
+
+def fp8_quant_per_channel_weights(w: torch.Tensor, wq: torch.Tensor | None = None,
+                                  s_w: torch.Tensor | None = None, stream=None):
+    """bf16 [N, K] -> (E4M3 codes uint8 [N, K], fp32 per-row scales [N])."""
+    N, K, ldw = _rows(w, "w")
+    if wq is None:
+        wq = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    if s_w is None:
+        s_w = torch.empty((N,), dtype=torch.float32, device=w.device)
+    _check(lib().fp8_quant_per_channel_weights(_ptr(w), N, K, ldw, _ptr(wq),
+                                               wq.stride(0) if N else K, _ptr(s_w),
+                                               _stream(stream)),
+           "fp8_quant_per_channel_weights")
+    return wq, s_w
+
+
+def fp8_scaled_gemm(xq: torch.Tensor, s_tok: torch.Tensor, wq: torch.Tensor,
+                    s_w: torch.Tensor, y: torch.Tensor | None = None, stream=None):
+    """(codes [M, K], scales [M]) x (codes [N, K], scales [N]) -> bf16 [M, N]."""
+    M, K = xq.shape
+    N = wq.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    _check(lib().fp8_scaled_gemm(_ptr(xq), _ptr(s_tok), _ptr(wq), _ptr(s_w), _ptr(y),
+                                 M, N, K, None, 0, _stream(stream)), "fp8_scaled_gemm")
+    return y
+
+
+def fp8_linear(x: torch.Tensor, wq: torch.Tensor, s_w: torch.Tensor,
+               y: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+               stream=None):
+    """The whole W8A8 layer: bf16 X [M, K] and offline-quantized W -> bf16 [M, N]."""
+    M, K = x.shape
+    N = wq.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    need = fp8_linear_workspace_size(M, N, K)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=x.device)
+    _check(lib().fp8_linear(_ptr(x), _ptr(wq), _ptr(s_w), _ptr(y), M, N, K,
+                            _ptr(workspace), workspace.numel(), _stream(stream)), "fp8_linear")
+    return y
+
+
+class QuantizedLinear:
+    """A bias-free linear layer whose weight was quantized once (per output
+    channel) by the library, and whose forward is fp8_linear.  The
+    workspace is kept and grown as needed; one instance must not be called
+    from two streams at once."""
+
+    def __init__(self, weight_bf16: torch.Tensor, stream=None):
+        self.out_features, self.in_features = weight_bf16.shape
+        self.wq, self.s_w = fp8_quant_per_channel_weights(weight_bf16, stream=stream)
+        self._ws = None
+
+    def __call__(self, x: torch.Tensor, y: torch.Tensor | None = None, stream=None):
+        need = fp8_linear_workspace_size(x.shape[0], self.out_features, self.in_features)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty((max(need, 1),), dtype=torch.uint8, device=x.device)
+        return fp8_linear(x, self.wq, self.s_w, y=y, workspace=self._ws, stream=stream)

@@ -1,0 +1,48 @@
+// Host-side interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Nothing here is exported from the shared library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace fp8k {
+
+// Per-row dynamic E4M3 quantization (quant.cu).  R > 0, K % 16 == 0.
+cudaError_t launch_quant_rows(const void* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q,
+                              int64_t ldq, float* s, cudaStream_t st);
+
+// Everything a scaled-GEMM launch needs.  xq [M, K] and wq [N, K] are
+// contiguous E4M3, y [M, N] contiguous bf16.
+struct GemmArgs {
+    const uint8_t* xq;
+    const float* s_tok;
+    const uint8_t* wq;
+    const float* s_w;
+    void* y;
+    int M, N, K;
+    unsigned* status;     // device status word
+    int num_sms;
+    bool pdl;             // launch as a programmatic dependent of the previous kernel
+    cudaStream_t stream;
+};
+
+// 2-D row-major uint8 tensor [rows, cols] (leading dimension ld_bytes) as a
+// TMA tensor map with a {box_cols, box_rows} box and 128-byte swizzle.
+// Returns false if the driver rejects it.  (api.cu)
+bool encode_tmap_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                    uint64_t ld_bytes, uint32_t box_cols, uint32_t box_rows);
+
+// Persistent 128x256-tile tcgen05 GEMM for large M (gemm_prefill.cu).
+cudaError_t launch_gemm_prefill(const GemmArgs& a);
+
+// Weight-streaming split-K tcgen05 GEMM for M <= 64 (gemm_decode.cu).
+constexpr int kDecodeMaxM = 64;
+cudaError_t launch_gemm_decode(const GemmArgs& a);
+
+// One-time per-device kernel attribute setup (dynamic shared memory limits).
+cudaError_t prepare_gemm_prefill();
+cudaError_t prepare_gemm_decode();
+
+}  // namespace fp8k

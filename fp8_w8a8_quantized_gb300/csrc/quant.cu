@@ -1,0 +1,209 @@
+// Dynamic per-row E4M3 quantization: one scale per row (a token of X, or an
+// output channel of W).
+//
+// Computes, for every row r of a bf16 matrix [R, K]:
+//   amax_r = max_k |x[r,k]|                      (exact, fp32)
+//   s_r    = amax_r / 448  (IEEE fp32 division), or 1 if amax_r == 0
+//   q[r,k] = E4M3_rn_satfinite(x[r,k] / s_r)     (IEEE fp32 quotient)
+// following "FP8 Inference Explained, in depth", "Scales and their
+// granularity" (s = amax / 448, x_fp8 = round(x / s)) and "Quantization: FP8
+// inference and KV-cache quantization", "Dynamic scales or static scales"
+// (per-token scales; saturating conversion).
+//
+// Layout of the work: a group of G threads owns a row; each thread keeps up
+// to 4 16-element chunks (two 16-byte loads each) of the row in registers
+// between the amax pass and the quantize pass, so X is read from HBM once.
+// The amax reduction is a butterfly of warp shuffles, then (G > 32) a pass
+// through shared memory.  Codes leave as one 16-byte store per chunk.
+// Very long rows (K > 65536) take a variant that streams the row twice.
+//
+// Memory-bound: 2 bytes in + 1 byte out per element (+4 bytes per row).
+// Divisions use __fdiv_rn (IEEE round-to-nearest); nothing here is compiled
+// with fast-math or flush-to-zero, so results are bit-identical to the fp32
+// definition above.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace fp8k {
+namespace {
+
+constexpr int kBlock = 256;  // threads per CTA for G <= 256
+constexpr int kVPT = 4;      // 16-element chunks per thread (register path)
+
+__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+__device__ __forceinline__ float amax8(const uint4& v, float m) {
+    m = fmaxf(m, fabsf(bf16lo(v.x)));
+    m = fmaxf(m, fabsf(bf16hi(v.x)));
+    m = fmaxf(m, fabsf(bf16lo(v.y)));
+    m = fmaxf(m, fabsf(bf16hi(v.y)));
+    m = fmaxf(m, fabsf(bf16lo(v.z)));
+    m = fmaxf(m, fabsf(bf16hi(v.z)));
+    m = fmaxf(m, fabsf(bf16lo(v.w)));
+    m = fmaxf(m, fabsf(bf16hi(v.w)));
+    return m;
+}
+
+// Two fp32 values -> two E4M3 codes (RN, saturating to +-448); `lo` lands in
+// the low byte (lower address).
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Four bf16 pairs (8 values) -> 8 codes packed in two 32-bit words.
+__device__ __forceinline__ uint2 quant8(const uint4& v, float s) {
+    uint2 o;
+    const uint32_t a = cvt_e4m3x2(__fdiv_rn(bf16lo(v.x), s), __fdiv_rn(bf16hi(v.x), s));
+    const uint32_t b = cvt_e4m3x2(__fdiv_rn(bf16lo(v.y), s), __fdiv_rn(bf16hi(v.y), s));
+    const uint32_t c = cvt_e4m3x2(__fdiv_rn(bf16lo(v.z), s), __fdiv_rn(bf16hi(v.z), s));
+    const uint32_t d = cvt_e4m3x2(__fdiv_rn(bf16lo(v.w), s), __fdiv_rn(bf16hi(v.w), s));
+    o.x = a | (b << 16);
+    o.y = c | (d << 16);
+    return o;
+}
+
+// Read-once 16-byte load that does not allocate in L1.
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float scale_of(float amax) {
+    return amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+}
+
+// Max over the G threads of a row group.  `red` holds one float per warp.
+template <int G, int B>
+__device__ __forceinline__ float group_max(float m, float* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if constexpr (G > 32) {
+        constexpr int WPG = G / 32;  // warps per group
+        const int warp = threadIdx.x >> 5;
+        if (lane_id() == 0) red[warp] = m;
+        __syncthreads();
+        const int first = (warp / WPG) * WPG;
+        m = red[first];
+#pragma unroll
+        for (int w = 1; w < WPG; ++w) m = fmaxf(m, red[first + w]);
+    }
+    return m;
+}
+
+template <int G>
+__global__ void __launch_bounds__(G > kBlock ? G : kBlock)
+    quant_rows_regs(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx,
+                    uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s) {
+    constexpr int B = G > kBlock ? G : kBlock;
+    constexpr int ROWS = B / G;
+    __shared__ float red[B / 32];
+    pdl_launch_dependents();
+
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * ROWS + threadIdx.x / G;
+    const int t = threadIdx.x % G;
+    const bool live = row < R;
+    const int64_t C = K >> 4;  // 16-element chunks per row
+
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (live ? row : 0) * ldx);
+    uint4 v[kVPT][2];
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kVPT; ++i) {
+        const int64_t c = t + static_cast<int64_t>(i) * G;
+        if (live && c < C) {
+            v[i][0] = ld_stream(xr + 2 * c);
+            v[i][1] = ld_stream(xr + 2 * c + 1);
+            m = amax8(v[i][1], amax8(v[i][0], m));
+        }
+    }
+    m = group_max<G, B>(m, red);
+    const float sc = scale_of(m);
+    if (!live) return;
+    uint4* qr = reinterpret_cast<uint4*>(q + row * ldq);
+#pragma unroll
+    for (int i = 0; i < kVPT; ++i) {
+        const int64_t c = t + static_cast<int64_t>(i) * G;
+        if (c < C) {
+            const uint2 a = quant8(v[i][0], sc);
+            const uint2 b = quant8(v[i][1], sc);
+            qr[c] = make_uint4(a.x, a.y, b.x, b.y);
+        }
+    }
+    if (t == 0) s[row] = sc;
+}
+
+// Rows longer than the register path holds: stream the row twice (the
+// second pass mostly hits L2).
+__global__ void __launch_bounds__(1024)
+    quant_rows_stream(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx,
+                      uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s) {
+    __shared__ float red[32];
+    pdl_launch_dependents();
+    const int64_t row = blockIdx.x;
+    const int64_t C = K >> 4;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + row * ldx);
+    float m = 0.0f;
+    for (int64_t c = threadIdx.x; c < C; c += 1024) {
+        const uint4 a = __ldg(xr + 2 * c), b = __ldg(xr + 2 * c + 1);
+        m = amax8(b, amax8(a, m));
+    }
+    m = group_max<1024, 1024>(m, red);
+    const float sc = scale_of(m);
+    uint4* qr = reinterpret_cast<uint4*>(q + row * ldq);
+    for (int64_t c = threadIdx.x; c < C; c += 1024) {
+        const uint2 a = quant8(ld_stream(xr + 2 * c), sc);
+        const uint2 b = quant8(ld_stream(xr + 2 * c + 1), sc);
+        qr[c] = make_uint4(a.x, a.y, b.x, b.y);
+    }
+    if (threadIdx.x == 0) s[row] = sc;
+}
+
+// K == 0: an empty row has amax 0, so its scale is 1.
+__global__ void fill_ones(float* s, int64_t R) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i < R) s[i] = 1.0f;
+}
+
+template <int G>
+cudaError_t launch_regs(const uint16_t* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q,
+                        int64_t ldq, float* s, cudaStream_t st) {
+    constexpr int B = G > kBlock ? G : kBlock;
+    constexpr int ROWS = B / G;
+    const int64_t grid = (R + ROWS - 1) / ROWS;
+    quant_rows_regs<G><<<static_cast<unsigned>(grid), B, 0, st>>>(x, R, K, ldx, q, ldq, s);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// Host launcher.  Preconditions (checked by the caller): R > 0, K % 16 == 0,
+// 16-byte aligned rows, R < 2^31.
+cudaError_t launch_quant_rows(const void* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q,
+                              int64_t ldq, float* s, cudaStream_t st) {
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    if (K == 0) {
+        fill_ones<<<static_cast<unsigned>((R + 255) / 256), 256, 0, st>>>(s, R);
+        return cudaGetLastError();
+    }
+    const int64_t C = K / 16;
+    if (C <= 32 * kVPT) return launch_regs<32>(xb, R, K, ldx, q, ldq, s, st);
+    if (C <= 64 * kVPT) return launch_regs<64>(xb, R, K, ldx, q, ldq, s, st);
+    if (C <= 128 * kVPT) return launch_regs<128>(xb, R, K, ldx, q, ldq, s, st);
+    if (C <= 256 * kVPT) return launch_regs<256>(xb, R, K, ldx, q, ldq, s, st);
+    if (C <= 512 * kVPT) return launch_regs<512>(xb, R, K, ldx, q, ldq, s, st);
+    if (C <= 1024 * kVPT) return launch_regs<1024>(xb, R, K, ldx, q, ldq, s, st);
+    quant_rows_stream<<<static_cast<unsigned>(R), 1024, 0, st>>>(xb, R, K, ldx, q, ldq, s);
+    return cudaGetLastError();
+}
+
+}  // namespace fp8k

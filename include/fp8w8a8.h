@@ -1,0 +1,171 @@
+/*
+ * fp8w8a8.h -- C ABI of the GB300 (sm_103a) FP8_DYNAMIC W8A8 linear layer.
+ *
+ * The layer (page titles and sections of the sources it follows):
+ *   "FP8 Inference Explained, in depth", "Inside a quantized linear layer":
+ *     weights are stored offline as E4M3 with one FP32 scale per output
+ *     channel; at run time a small kernel finds each token's amax, divides
+ *     and casts the activations to E4M3; the tensor cores multiply E4M3 by
+ *     E4M3 and accumulate in FP32; both scales are constant along K, so
+ *     y[m,n] = s_tok[m] * s_w[n] * sum_k q_x[m,k] * q_w[n,k].
+ *   "FP8 Inference Explained, in depth", "Scales and their granularity":
+ *     x_fp8 = round(x / s) with s = amax / 448.
+ *   "FP8 Quantization", "How FP8 Matmul Works at the Hardware Level":
+ *     FP8 x FP8 -> FP32 accumulate -> BF16 output.
+ *
+ * Numerics of every quantizing entry point (bit-exact, deterministic):
+ *   amax = max_k |x[k]| in fp32 (bf16 inputs widen exactly);
+ *   s    = amax / 448 as an IEEE fp32 division (round to nearest even),
+ *          or s = 1 when amax == 0;
+ *   q[k] = E4M3(x[k] / s): IEEE fp32 quotient, then round to nearest even
+ *          onto the float8_e4m3fn grid, saturating at +-448 (0x7E / 0xFE),
+ *          subnormals down to 2^-9, the sign of zero kept.
+ *   NaN or Inf inputs are outside the contract.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers marked "device" are CUDA device pointers owned by the caller
+ *     (for example PyTorch-allocated).  The library never allocates, frees or
+ *     keeps them after the call returns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call is asynchronous on that stream and never
+ *     synchronizes the host.
+ *   - Layouts are row-major.  Activations X are [M, K] (tokens x in-features),
+ *     weights W are [N, K] (out-features x in-features, the nn.Linear layout,
+ *     K contiguous), outputs Y are [M, N] bf16 with leading dimension N.
+ *   - Host-side argument checks run before any launch; a rejected call
+ *     launches nothing and returns FP8_ERR_INVALID_ARG or FP8_ERR_UNSUPPORTED.
+ *     M == 0 or N == 0 is a valid no-op and returns FP8_OK.
+ *   - The current CUDA device must be the one that owns the pointers; it must
+ *     be a compute capability 10.3 (GB300) device, else FP8_ERR_UNSUPPORTED.
+ *   - A launch failure returns FP8_ERR_CUDA.  Device-side waits are bounded:
+ *     a kernel whose wait runs out records it in a device status word and
+ *     exits; fp8_device_status() reports it as FP8_ERR_TIMEOUT.
+ */
+#ifndef FP8W8A8_H
+#define FP8W8A8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FP8_API __attribute__((visibility("default")))
+#else
+#define FP8_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8_OK = 0,
+    FP8_ERR_INVALID_ARG = 1,  /* null pointer, negative size, ld < K, ...    */
+    FP8_ERR_UNSUPPORTED = 2,  /* alignment/size outside what the kernels take,
+                                 or not a GB300 device                        */
+    FP8_ERR_WORKSPACE = 3,    /* workspace missing, misaligned or too small   */
+    FP8_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed            */
+    FP8_ERR_TIMEOUT = 5       /* a device-side wait ran out (see
+                                 fp8_device_status)                           */
+} fp8_status_t;
+
+/*
+ * Dynamic per-token activation quantization.
+ * Source: "FP8 Inference Explained, in depth", "Scales and their
+ * granularity" (s = amax / 448, x_fp8 = round(x / s)); "Quantization: FP8
+ * inference and KV-cache quantization", "Dynamic scales or static scales"
+ * (one scale per token, recomputed on every forward pass).
+ *
+ *   x_bf16 [device, in]  bf16 [M, K], leading dimension ldx (elements)
+ *   M, K                 tokens, in-features; M >= 0, K >= 0
+ *   ldx                  >= K, multiple of 8 (16-byte rows)
+ *   xq     [device, out] E4M3 codes [M, K], leading dimension ldq (bytes)
+ *   ldq                  >= K, multiple of 16
+ *   s_tok  [device, out] fp32 [M], the dequant scale of each token
+ * Requirements: K % 16 == 0; x_bf16 and xq 16-byte aligned; s_tok 4-byte
+ * aligned.  K == 0 writes s_tok = 1.
+ */
+FP8_API fp8_status_t fp8_quant_per_token(const void* x_bf16, int64_t M, int64_t K,
+                                         int64_t ldx, uint8_t* xq, int64_t ldq, float* s_tok,
+                                         void* stream);
+
+/*
+ * Static per-output-channel weight quantization (run once, offline): the
+ * same rule as fp8_quant_per_token applied to each row of W [N, K].
+ * Source: "FP8 Quantization", "Granularity" (per-channel: one scale per
+ * output row) and "Implementation" (FP8_DYNAMIC: weights quantized
+ * statically per channel offline).
+ *
+ *   w_bf16 [device, in]  bf16 [N, K], leading dimension ldw (elements)
+ *   wq     [device, out] E4M3 codes [N, K], leading dimension ldwq (bytes)
+ *   s_w    [device, out] fp32 [N]
+ * Requirements as for fp8_quant_per_token (with N for M).
+ */
+FP8_API fp8_status_t fp8_quant_per_channel_weights(const void* w_bf16, int64_t N, int64_t K,
+                                                   int64_t ldw, uint8_t* wq, int64_t ldwq,
+                                                   float* s_w, void* stream);
+
+/*
+ * Scaled FP8 GEMM with the dequant epilogue fused:
+ *   y[m, n] = bf16_rn( (acc[m, n] * s_tok[m]) * s_w[n] ),
+ *   acc[m, n] = sum_k e4m3(xq[m, k]) * e4m3(wq[n, k])   (fp32 accumulation)
+ * Source: "FP8 Inference Explained, in depth", "Inside a quantized linear
+ * layer"; "FP8 Quantization", "How FP8 Matmul Works at the Hardware Level".
+ *
+ *   xq     [device, in]  E4M3 [M, K], contiguous (leading dimension K)
+ *   s_tok  [device, in]  fp32 [M]
+ *   wq     [device, in]  E4M3 [N, K], contiguous (leading dimension K)
+ *   s_w    [device, in]  fp32 [N]
+ *   y_bf16 [device, out] bf16 [M, N], contiguous
+ *   workspace, ws_bytes  unused by the current kernels (may be NULL / 0);
+ *                        fp8_scaled_gemm_workspace_size() returns 0.
+ * Requirements: K % 16 == 0, K > 0; xq, wq, y_bf16 16-byte aligned;
+ * M, N, K < 2^31.  The fp32 summation order is fixed for a given shape, so
+ * repeated calls give identical bits.
+ * Kernel choice: M <= 64 uses the weight-streaming split-K kernel (weights on
+ * the 128-row MMA side, tokens on the narrow side), larger M the persistent
+ * 128x256-tile kernel.
+ */
+FP8_API fp8_status_t fp8_scaled_gemm(const uint8_t* xq, const float* s_tok, const uint8_t* wq,
+                                     const float* s_w, void* y_bf16, int64_t M, int64_t N,
+                                     int64_t K, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * The whole W8A8 linear layer: fp8_quant_per_token on X into the workspace,
+ * then fp8_scaled_gemm, on `stream`, as two launches (the second may start
+ * its prologue and weight prefetch while the first finishes).
+ *
+ *   x_bf16 [device, in]  bf16 [M, K], contiguous
+ *   wq, s_w              as for fp8_scaled_gemm (offline-quantized weights)
+ *   y_bf16 [device, out] bf16 [M, N], contiguous
+ *   workspace [device]   at least fp8_linear_workspace_size(M, N, K) bytes,
+ *                        256-byte aligned; holds xq [M, K] then s_tok [M].
+ *                        Its contents after the call are the quantized
+ *                        activations and their scales.  It must not be in
+ *                        use by another call in flight.
+ * Requirements: as for the two calls it makes.
+ */
+FP8_API fp8_status_t fp8_linear(const void* x_bf16, const uint8_t* wq, const float* s_w,
+                                void* y_bf16, int64_t M, int64_t N, int64_t K, void* workspace,
+                                size_t ws_bytes, void* stream);
+
+/* Workspace bytes fp8_linear needs for an [M, K] x [N, K]^T layer:
+ * round_up(M*K, 256) + round_up(4*M, 256).  0 for invalid sizes. */
+FP8_API size_t fp8_linear_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/* Workspace bytes fp8_scaled_gemm needs (currently always 0). */
+FP8_API size_t fp8_scaled_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/* Static, NUL-terminated name of a status code; never NULL. */
+FP8_API const char* fp8_status_string(fp8_status_t status);
+
+/* Device status word of the current device: FP8_OK, or FP8_ERR_TIMEOUT if a
+ * kernel of this library gave up a bounded wait since the last clear.  Reads
+ * the word with a synchronous copy (it waits for the device); clear != 0
+ * resets it.  Returns FP8_ERR_CUDA if the copy fails. */
+FP8_API fp8_status_t fp8_device_status(int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8W8A8_H */

@@ -1,0 +1,96 @@
+"""The C-ABI library loads and exports every entry point include/*.h
+declares; host-side argument checks answer without touching a GPU (CPU only:
+no call here reaches a kernel launch)."""
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def L():
+    from fp8_w8a8_quantized_gb300 import build
+    build.build()
+    import fp8_w8a8_quantized_gb300 as pkg
+    return pkg.lib()
+
+
+def declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names.update(re.findall(r"FP8_API\s+[\w\s\*]+?\b(fp8_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_symbols()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_exported_symbols_are_only_the_abi(L):
+    from fp8_w8a8_quantized_gb300 import LIBRARY_PATH
+    out = subprocess.run(["nm", "-D", "--defined-only", LIBRARY_PATH],
+                         capture_output=True, text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    fp8 = {s for s in exported if s.startswith("fp8_")}
+    assert fp8 == set(declared_symbols())
+
+
+def test_status_strings(L):
+    import fp8_w8a8_quantized_gb300 as pkg
+    for code, name in pkg._binding.STATUS_NAMES.items():
+        assert pkg.fp8_status_string(code) == name
+    assert pkg.fp8_status_string(77) == "FP8_ERR_UNKNOWN"
+
+
+def test_workspace_size(L):
+    import fp8_w8a8_quantized_gb300 as pkg
+    assert pkg.fp8_linear_workspace_size(1, 4096, 4096) == 4096 + 256
+    assert pkg.fp8_linear_workspace_size(3, 10, 48) == 256 + 256
+    assert pkg.fp8_linear_workspace_size(0, 10, 48) == 0
+    assert pkg.fp8_linear_workspace_size(-1, 10, 48) == 0
+    assert L.fp8_scaled_gemm_workspace_size(32, 4096, 4096) == 0
+
+
+def test_host_checks_reject_before_any_launch(L):
+    # null pointers, negative sizes, bad leading dimensions, K not a multiple
+    # of 16, misaligned pointers: all answered on the host
+    INVALID, UNSUP, WS = 1, 2, 3
+    fake = 1 << 20  # never dereferenced: every call below is rejected first
+    assert L.fp8_quant_per_token(None, 4, 32, 32, fake, 32, fake, None) == INVALID
+    assert L.fp8_quant_per_token(fake, -1, 32, 32, fake, 32, fake, None) == INVALID
+    assert L.fp8_quant_per_token(fake, 4, 32, 16, fake, 32, fake, None) == INVALID
+    assert L.fp8_quant_per_token(fake, 4, 24, 24, fake, 32, fake, None) == UNSUP
+    assert L.fp8_quant_per_token(fake + 8, 4, 32, 32, fake, 32, fake, None) == UNSUP
+    assert L.fp8_quant_per_token(fake, 4, 32, 36, fake, 32, fake, None) == UNSUP
+    assert L.fp8_quant_per_token(fake, 0, 32, 32, fake, 32, fake, None) == 0
+    assert L.fp8_quant_per_channel_weights(fake, 4, 32, 32, None, 32, fake, None) == INVALID
+    assert L.fp8_scaled_gemm(None, fake, fake, fake, fake, 4, 4, 32, None, 0, None) == INVALID
+    assert L.fp8_scaled_gemm(fake, fake, fake, fake, fake, 4, 4, 40, None, 0, None) == UNSUP
+    assert L.fp8_scaled_gemm(fake, fake, fake, fake, fake + 4, 4, 4, 32, None, 0, None) == UNSUP
+    assert L.fp8_scaled_gemm(fake, fake, fake, fake, fake, 0, 4, 32, None, 0, None) == 0
+    assert L.fp8_scaled_gemm(fake, fake, fake, fake, fake, 4, 0, 32, None, 0, None) == 0
+    assert L.fp8_scaled_gemm(fake, fake, fake, fake, fake, 4, 4, -16, None, 0, None) == INVALID
+    assert L.fp8_linear(fake, fake, fake, fake, 4, 4, 32, None, 0, None) == WS
+    assert L.fp8_linear(fake, fake, fake, fake, 4, 4, 32, fake, 10, None) == WS
+    assert L.fp8_linear(fake, fake, fake, fake, 4, 4, 32, fake + 16, 4096, None) == WS
+    assert L.fp8_linear(fake, fake, fake, fake, 4, 4, 20, fake, 4096, None) == UNSUP
+    assert L.fp8_linear(fake, fake, fake, fake, 0, 4, 32, None, 0, None) == 0
+    assert L.fp8_linear(fake, None, fake, fake, 4, 4, 32, fake, 4096, None) == INVALID
+    assert L.fp8_linear(fake, fake, fake, fake, 1 << 40, 4, 32, fake, 4096, None) == INVALID
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg_dir = os.path.join(ROOT, "fp8_w8a8_quantized_gb300")
+    for path in glob.glob(os.path.join(pkg_dir, "**", "*"), recursive=True):
+        if os.path.isfile(path) and path.endswith((".py", ".cu", ".cuh", ".h")):
+            text = open(path).read()
+            assert "import oracle" not in text and "from oracle" not in text, path
+            assert "fp8_oracle" not in text and "orc_" not in text, path

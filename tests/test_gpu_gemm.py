@@ -1,0 +1,121 @@
+"""GPU parity of the scaled FP8 GEMM (both kernels: the weight-streaming
+split-K kernel for M <= 64 and the persistent tile kernel above), fed with the
+oracle's own codes and scales, against the oracle's fp64 result."""
+import numpy as np
+import pytest
+import torch
+
+import fp8_w8a8_quantized_gb300 as pkg
+from parity import check_rows
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+FINITE = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def run_gemm(qx, s_tok, qw, s_w):
+    y = pkg.fp8_scaled_gemm(dev(qx), dev(s_tok), dev(qw), dev(s_w))
+    torch.cuda.synchronize()
+    assert pkg.fp8_device_status() == 0
+    return y.double().cpu().numpy()
+
+
+def random_operands(M, N, K, seed):
+    rng = np.random.default_rng(seed)
+    qx = rng.choice(FINITE, size=(M, K))
+    qw = rng.choice(FINITE, size=(N, K))
+    s_tok = np.exp2(rng.uniform(-12, 4, M)).astype(np.float32)
+    s_w = np.exp2(rng.uniform(-12, 0, N)).astype(np.float32)
+    return qx, s_tok, qw, s_w
+
+
+SHAPES = [  # (M, N, K): ragged edges, single k-block, many k-blocks, both kernels
+    (1, 8, 16), (1, 128, 128), (3, 24, 48), (16, 256, 256), (17, 100, 272), (32, 264, 1024),
+    (33, 1000, 4096), (64, 384, 2048), (65, 256, 256), (128, 256, 128), (129, 520, 1040),
+    (200, 300, 4112), (256, 512, 4096), (300, 1000, 1024), (513, 777, 2064),
+]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_random_codes(oracle_mod, M, N, K):
+    qx, s_tok, qw, s_w = random_operands(M, N, K, M * 1000 + N + K)
+    y = run_gemm(qx, s_tok, qw, s_w)
+    ref = oracle_mod.scaled_gemm(qx, s_tok, qw, s_w)
+    check_rows(y, ref, f"gemm {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M", [1, 8, 32, 64, 128, 1024])
+def test_all_positive_long_k_accumulation(oracle_mod, M):
+    # all products positive and large: exposes any loss of accumulator bits
+    # at the longest K the layers use (fp32 accumulation keeps 24 bits)
+    K, N = 28672, 256
+    rng = np.random.default_rng(M)
+    qx = rng.integers(0x70, 0x7F, size=(M, K), dtype=np.uint8)
+    qw = rng.integers(0x30, 0x40, size=(N, K), dtype=np.uint8)
+    s_tok = np.full(M, 1e-3, dtype=np.float32)
+    s_w = np.full(N, 1e-4, dtype=np.float32)
+    y = run_gemm(qx, s_tok, qw, s_w)
+    ref = oracle_mod.scaled_gemm(qx, s_tok, qw, s_w)
+    rel = np.max(np.abs(y - ref) / np.abs(ref))
+    assert rel < 4e-3, rel
+
+
+def test_identity_like_columns(oracle_mod):
+    # W rows are one-hot (code 1.0 at column n % K): y picks one x value per n,
+    # so any row/column/k mix-up in tiling shows as a wrong exact value
+    M, N, K = 130, 300, 512
+    rng = np.random.default_rng(5)
+    qx = rng.choice(FINITE, size=(M, K))
+    qw = np.zeros((N, K), dtype=np.uint8)
+    qw[np.arange(N), np.arange(N) % K] = 0x38
+    s_tok = np.ones(M, dtype=np.float32)
+    s_w = np.ones(N, dtype=np.float32)
+    for m_sub in (M, 7):
+        y = run_gemm(qx[:m_sub], s_tok[:m_sub], qw, s_w)
+        ref = oracle_mod.scaled_gemm(qx[:m_sub], s_tok[:m_sub], qw, s_w)
+        # every output is a single e4m3 value: exact in bf16
+        assert np.array_equal(y, ref), m_sub
+
+
+def test_deterministic_bits():
+    qx, s_tok, qw, s_w = random_operands(32, 4096, 4096, 1)
+    assert np.array_equal(run_gemm(qx, s_tok, qw, s_w), run_gemm(qx, s_tok, qw, s_w))
+    qx, s_tok, qw, s_w = random_operands(300, 1024, 4096, 2)
+    assert np.array_equal(run_gemm(qx, s_tok, qw, s_w), run_gemm(qx, s_tok, qw, s_w))
+
+
+@pytest.mark.parametrize("M", [5, 200])
+def test_output_guard_bands(oracle_mod, M):
+    N, K = 136, 256
+    qx, s_tok, qw, s_w = random_operands(M, N, K, 77)
+    pad = 64
+    buf = torch.full((pad + M * N + pad,), -12345.0, dtype=torch.bfloat16, device=DEV)
+    y = buf[pad:pad + M * N]
+    a, b, c, d = dev(qx), dev(s_tok), dev(qw), dev(s_w)
+    st = pkg.lib().fp8_scaled_gemm(a.data_ptr(), b.data_ptr(), c.data_ptr(), d.data_ptr(),
+                                   y.data_ptr(), M, N, K, None, 0,
+                                   torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    bb = buf.float().cpu().numpy()
+    assert np.all(bb[:pad] == -12345.0) and np.all(bb[pad + M * N:] == -12345.0)
+    check_rows(y.view(M, N).double().cpu().numpy(),
+               oracle_mod.scaled_gemm(qx, s_tok, qw, s_w), "guarded")
+
+
+def test_empty_and_rejected_calls():
+    L = pkg.lib()
+    x = torch.zeros(64, 64, dtype=torch.uint8, device=DEV)
+    f = torch.ones(64, dtype=torch.float32, device=DEV)
+    y = torch.zeros(64, 64, dtype=torch.bfloat16, device=DEV)
+    s = torch.cuda.current_stream().cuda_stream
+    assert L.fp8_scaled_gemm(x.data_ptr(), f.data_ptr(), x.data_ptr(), f.data_ptr(),
+                             y.data_ptr(), 0, 64, 64, None, 0, s) == 0
+    assert L.fp8_scaled_gemm(x.data_ptr(), f.data_ptr(), x.data_ptr(), f.data_ptr(),
+                             y.data_ptr() + 2, 4, 4, 64, None, 0, s) == 2
+    torch.cuda.synchronize()
+    assert torch.all(y == 0)
