@@ -1,0 +1,442 @@
+#!/usr/bin/env python3
+"""Benchmark of the FP8_DYNAMIC W8A8 linear layer on one GB300 (per rank).
+
+One *step* is one pass of the whole hot path (per-token quantization, FP8
+GEMM, dequant epilogue -- i.e. fp8_linear) over every layer of the workload:
+Llama-3.1-8B-shaped decode layers, M in {1, 8, 32} tokens x (K, N) in
+{(4096, 6144) QKV, (4096, 4096) O, (4096, 28672) gate/up, (14336, 4096)
+down}: 12 fp8_linear calls.  The metric is algorithmic bytes / second
+(2MK activations + NK E4M3 weights + 4N weight scales + 2MN outputs per
+call).  Weights are rotated over enough sets that their footprint is more
+than twice the L2 cache, so every step streams its weights from HBM.
+
+Printed (rank 0, one JSON line): value (device-timed, inputs resident),
+e2e (same metric through the public API with pinned host inputs/outputs
+copied in the timed region), roofline of the dominant kernel (the decode
+GEMM), prefill TFLOPS of the 8B prefill shapes as context, the CPU oracle
+timed on a bounded sample, and the SM clocks seen during the timed region.
+
+--impl reference times the CPU oracle itself on the same workload.
+N > 1 (torchrun): the layer does not shard, so each rank runs an independent
+replica; value = all ranks' bytes / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fp8_linear TFLOPS & % FP8 peak (prefill); GB/s & % HBM (decode M≤32)"
+WORKLOAD = ("llama-3.1-8b decode linear layers: M in {1,8,32} x (K,N) in "
+            "{(4096,6144),(4096,4096),(4096,28672),(14336,4096)}")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_PER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor-core ratio (4.5 / 2.25 PFLOP/s)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def decode_calls():
+    from fp8_w8a8_quantized_gb300 import workloads
+    return [(M, K, N) for M in workloads.DECODE_M for (_, K, N) in workloads.SHAPES_8B]
+
+
+def layer_bytes(M, K, N):
+    return 2 * M * K + N * K + 4 * N + 2 * M * N
+
+
+def gemm_bytes(M, K, N):
+    return M * K + 4 * M + N * K + 4 * N + 2 * M * N
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def setup_dist(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_inputs(calls):
+    """Host copies of the same synthetic inputs, with the weights quantized
+    offline by the oracle (not part of the timed work)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from fp8_w8a8_quantized_gb300 import workloads
+    oracle.build()
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    wcache, items = {}, []
+    for (M, K, N) in calls:
+        if (K, N) not in wcache:
+            w = workloads.weights(N, K, workloads.SEED_DECODE, "cpu")
+            wcache[(K, N)] = oracle.quant_rows_bf16(bits(w))
+        x = workloads.gaussian_outliers(M, K, workloads.SEED_DECODE, "cpu")
+        items.append((M, K, N, bits(x)) + wcache[(K, N)])
+    return items
+
+
+def oracle_step(items):
+    import oracle
+    for (M, K, N, xb, qw, sw) in items:
+        oracle.linear(xb, qw, sw)
+
+
+def time_oracle(calls, budget_s: float, min_reps: int = 1):
+    """Run whole oracle steps until `budget_s` is spent (at least min_reps)."""
+    import oracle
+    items = oracle_inputs(calls)
+    nbytes = sum(layer_bytes(M, K, N) for (M, K, N) in calls)
+    reps, t0 = 0, time.perf_counter()
+    while reps < min_reps or time.perf_counter() - t0 < budget_s:
+        oracle_step(items)
+        reps += 1
+    dt = time.perf_counter() - t0
+    return {"value": nbytes * reps / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "s_per_step": dt / reps, "reps": reps}
+
+
+def run_reference(args):
+    world, rank, _ = setup_dist(args)
+    if rank != 0:
+        return 0
+    calls = decode_calls()
+    import oracle
+    all_items = oracle_inputs(calls)
+    # bounded sample: the longest prefix of the step's calls whose oracle time
+    # keeps the whole run (warmup + steps) within about two minutes
+    per_call = []
+    for it in all_items:
+        t0 = time.perf_counter()
+        oracle_step([it])
+        per_call.append(time.perf_counter() - t0)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n, acc = 0, 0.0
+    while n < len(all_items) and (n == 0 or acc + per_call[n] <= budget):
+        acc += per_call[n]
+        n += 1
+    items = all_items[:n]
+    sample = ("the whole step (all 12 layer calls)" if n == len(all_items) else
+              f"the first {n} of the step's 12 layer calls (M, K, N) = "
+              f"{[c[:3] for c in items]}")
+    nbytes = sum(layer_bytes(M, K, N) for (M, K, N, *_rest) in items)
+    for _ in range(args.warmup):
+        oracle_step(items)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(items)
+    dt = time.perf_counter() - t0
+    value = nbytes * args.steps / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int64 (exact E4M3 products) + f64 epilogue",
+        "data": "synthetic", "config": {"workload": WORKLOAD},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+
+    import fp8_w8a8_quantized_gb300 as pkg
+    from fp8_w8a8_quantized_gb300 import build, workloads
+
+    world, rank, local = setup_dist(args)
+    build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
+    pk, pk_kind = peaks()
+    calls = decode_calls()
+
+    # weights: rotate enough sets that the footprint exceeds 2 x L2
+    per_set = sum(N * K for (_, K, N) in workloads.SHAPES_8B)
+    nsets = max(2, -(-2 * l2 // per_set) + 1)
+    wsets = []
+    for s in range(nsets):
+        d = {}
+        for (_, K, N) in workloads.SHAPES_8B:
+            w = workloads.weights(N, K, workloads.SEED_DECODE + 100 * s, dev)
+            d[(K, N)] = pkg.fp8_quant_per_channel_weights(w)
+            del w
+        wsets.append(d)
+    xs = [workloads.gaussian_outliers(M, K, workloads.SEED_DECODE, dev) for (M, K, N) in calls]
+    ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for (M, K, N) in calls]
+    wss = [torch.empty(pkg.fp8_linear_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+           for (M, K, N) in calls]
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.Stream(dev)
+    nbytes_step = sum(layer_bytes(M, K, N) for (M, K, N) in calls)
+
+    def step_linear(wset, s):
+        for i, (M, K, N) in enumerate(calls):
+            wq, sw = wset[(K, N)]
+            pkg.fp8_linear(xs[i], wq, sw, y=ys[i], workspace=wss[i], stream=s)
+
+    # one CUDA graph per weight set: a step is one replay
+    graphs = []
+    with torch.cuda.stream(stream):
+        for wset in wsets:
+            step_linear(wset, stream)  # warm (per-device setup happens here)
+        stream.synchronize()
+        for wset in wsets:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step_linear(wset, torch.cuda.current_stream())
+            graphs.append(g)
+    torch.cuda.synchronize()
+
+    def timed(fn_step, steps, warmup):
+        with torch.cuda.stream(stream):
+            for i in range(warmup):
+                fn_step(i)
+        stream.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(steps):
+                fn_step(i)
+            e1.record(stream)
+        e1.synchronize()
+        torch.cuda.synchronize()
+        barrier(world)
+        return e0.elapsed_time(e1) / 1e3
+
+    replay = lambda i: graphs[i % nsets].replay()
+    with ClockSampler(local) as clk:
+        t_main = timed(replay, args.steps, max(args.warmup, 3))
+    t_main = max_over_ranks(t_main, world)
+    value = world * nbytes_step * args.steps / t_main / 1e9
+
+    # --- dominant kernel alone: the decode GEMM over the same 12 shapes ----
+    qx = [pkg.fp8_quant_per_token(x) for x in xs]
+    gemm_graphs = []
+    with torch.cuda.stream(stream):
+        for wset in wsets:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i, (M, K, N) in enumerate(calls):
+                    wq, sw = wset[(K, N)]
+                    pkg.fp8_scaled_gemm(qx[i][0], qx[i][1], wq, sw, y=ys[i],
+                                        stream=torch.cuda.current_stream())
+            gemm_graphs.append(g)
+    gsteps = max(args.steps, 50)
+    t_gemm = timed(lambda i: gemm_graphs[i % nsets].replay(), gsteps, 3)
+    gbytes = sum(gemm_bytes(M, K, N) for (M, K, N) in calls)
+    achieved = gbytes * gsteps / t_gemm / 1e9
+    hbm_peak = pk["hbm_gbs"]
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "traffic": GEMM_DECODE_TRAFFIC,
+                "kernel": "gemm_decode_kernel", "peak_kind": f"{pk_kind} copy bandwidth",
+                "frac_of_8tbs_spec": achieved / 8000.0}
+
+    # --- prefill context: 8B shapes at M = 2048, 8192 (TFLOPS) -------------
+    pre_calls = [(M, K, N) for M in workloads.PREFILL_M for (_, K, N) in workloads.SHAPES_8B]
+    pxs = {}
+    for (M, K, N) in pre_calls:
+        if (M, K) not in pxs:
+            pxs[(M, K)] = workloads.student_t_outliers(M, K, workloads.SEED_PREFILL, dev)
+    pys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for (M, K, N) in pre_calls]
+    pws = torch.empty(max(pkg.fp8_linear_workspace_size(M, N, K) for (M, K, N) in pre_calls),
+                      dtype=torch.uint8, device=dev)
+    wset0 = wsets[0]
+
+    def prefill_step(i):
+        for j, (M, K, N) in enumerate(pre_calls):
+            wq, sw = wset0[(K, N)]
+            pkg.fp8_linear(pxs[(M, K)], wq, sw, y=pys[j], workspace=pws, stream=stream)
+
+    psteps = max(3, min(args.steps, 20))
+    t_pre = timed(prefill_step, psteps, 2)
+    flops = sum(2 * M * N * K for (M, K, N) in pre_calls)
+    tflops = flops * psteps / t_pre / 1e12
+    fp8_peak = FP8_PER_BF16 * pk["bf16_tflops_sustained"]
+    prefill = {"tflops": tflops, "peak_tflops": fp8_peak,
+               "peak_kind": f"2 x {pk_kind} sustained bf16 (nominal fp8/bf16 ratio)",
+               "frac": tflops / fp8_peak, "frac_of_4500_nominal": tflops / 4500.0,
+               "workload": "llama-3.1-8b prefill layers, M in {2048,8192}, 8 fp8_linear calls"}
+    del pxs, pys, pws
+
+    # --- e2e: public API with pinned host buffers, copies in the timed region
+    hx = [x.cpu().pin_memory() for x in xs]
+    hy = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys]
+    dx = [torch.empty_like(x) for x in xs]
+    h2d = sum(x.numel() * x.element_size() for x in xs)
+    d2h = sum(y.numel() * y.element_size() for y in ys)
+
+    def e2e_step(i):
+        wset = wsets[i % nsets]
+        for j, (M, K, N) in enumerate(calls):
+            dx[j].copy_(hx[j], non_blocking=True)
+            wq, sw = wset[(K, N)]
+            pkg.fp8_linear(dx[j], wq, sw, y=ys[j], workspace=wss[j], stream=stream)
+            hy[j].copy_(ys[j], non_blocking=True)
+
+    esteps = max(args.steps, 20)
+    t_e2e = max_over_ranks(timed(e2e_step, esteps, 3), world)
+    e2e = {"value": world * nbytes_step * esteps / t_e2e / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "how": "fp8_linear called from Python per layer, no graph"}
+
+    if pkg.fp8_device_status() != pkg.FP8_OK:
+        raise RuntimeError("a kernel gave up a bounded wait during the benchmark")
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cb = time_oracle(calls, budget_s=args.cpu_budget)
+        cpu = {"value": cb["value"], "unit": "GB/s", "cores": cb["cores"], "kind": "oracle",
+               "sample": f"whole decode step (12 layer calls), {cb['reps']} step(s), "
+                         f"{cb['s_per_step']:.2f} s per step"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": t_main / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate)",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "weight_sets": nsets,
+                       "weight_bytes_per_set": per_set,
+                       "l2_policy": f"inputs larger than L2: weights rotated over {nsets} sets "
+                                    f"({nsets * per_set / 2**20:.0f} MiB > 2 x L2)",
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "frac_of_hbm": value / hbm_peak, "frac_of_8tbs_spec": value / 8000.0},
+            "gpu_launches": 2 * len(calls) * args.steps,
+            "roofline": roofline,
+            "prefill": prefill,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+# Per-launch DRAM traffic of the decode GEMM from an ncu capture of the same
+# kernel build (None until captured, and again whenever the kernel changes).
+GEMM_DECODE_TRAFFIC = None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle work for cpu_baseline")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

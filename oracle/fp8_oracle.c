@@ -232,11 +232,10 @@ void orc_gemm_exact(const uint8_t* qx, int64_t ldqx, const uint8_t* qw, int64_t 
     int i;
     for (i = 0; i < 256; ++i)
         tab[i] = ((i & 0x7F) == 0x7F) ? 0 : code_times_512((uint8_t)i);
-#pragma omp parallel for schedule(dynamic, 1)
+#pragma omp parallel for collapse(2) schedule(static)
     for (m = 0; m < M; ++m) {
-        int64_t n, k;
-        for (n = 0; n < N; ++n) {
-            int64_t sum = 0;
+        for (int64_t n = 0; n < N; ++n) {
+            int64_t sum = 0, k;
             for (k = 0; k < K; ++k)
                 sum += tab[qx[m * ldqx + k]] * tab[qw[n * ldqw + k]];
             acc[m * N + n] = sum;

@@ -93,7 +93,7 @@ def test_output_guard_bands(oracle_mod, M):
     N, K = 136, 256
     qx, s_tok, qw, s_w = random_operands(M, N, K, 77)
     pad = 64
-    buf = torch.full((pad + M * N + pad,), -12345.0, dtype=torch.bfloat16, device=DEV)
+    buf = torch.full((pad + M * N + pad,), -12288.0, dtype=torch.bfloat16, device=DEV)
     y = buf[pad:pad + M * N]
     a, b, c, d = dev(qx), dev(s_tok), dev(qw), dev(s_w)
     st = pkg.lib().fp8_scaled_gemm(a.data_ptr(), b.data_ptr(), c.data_ptr(), d.data_ptr(),
@@ -102,7 +102,7 @@ def test_output_guard_bands(oracle_mod, M):
     assert st == 0
     torch.cuda.synchronize()
     bb = buf.float().cpu().numpy()
-    assert np.all(bb[:pad] == -12345.0) and np.all(bb[pad + M * N:] == -12345.0)
+    assert np.all(bb[:pad] == -12288.0) and np.all(bb[pad + M * N:] == -12288.0)
     check_rows(y.view(M, N).double().cpu().numpy(),
                oracle_mod.scaled_gemm(qx, s_tok, qw, s_w), "guarded")
 
