@@ -148,6 +148,32 @@ FP8_API fp8_status_t fp8_linear(const void* x_bf16, const uint8_t* wq, const flo
                                 void* y_bf16, int64_t M, int64_t N, int64_t K, void* workspace,
                                 size_t ws_bytes, void* stream);
 
+/*
+ * fp8_linear for callers that cannot allocate device memory (no workspace
+ * argument; the call allocates nothing).  The pages have no counterpart:
+ * this is a convenience of this library.
+ *
+ * Who needs it: code that may not create device allocations of its own, such
+ * as a plugin inside a host application that owns all device memory, or a
+ * latency-critical loop in which cudaMalloc / cudaFree (which can synchronize
+ * the device) must not run.  The quantized activations and scales go to a
+ * fixed array of FP8_STATIC_SCRATCH_BYTES inside the library instead; every
+ * GPU that loads the library holds that array until the process exits.
+ *
+ *   x_bf16, wq, s_w, y_bf16, M, N, K, stream   as for fp8_linear.
+ * Limit: round_up(M*K, 256) + round_up(4*M, 256) <= FP8_STATIC_SCRATCH_BYTES,
+ * else FP8_ERR_WORKSPACE and nothing is launched.
+ * The first call on each device does a one-time set-up (it looks up the
+ * array's device address with that device current); make that first call
+ * before any stream capture.  All calls on a device share the array and it
+ * keeps the last call's contents: calls that overlap on the GPU (two streams
+ * at once) race on it.  Nothing in it needs to start at zero.
+ */
+#define FP8_STATIC_SCRATCH_BYTES (8u << 20)
+FP8_API fp8_status_t fp8_linear_static_scratch(const void* x_bf16, const uint8_t* wq,
+                                               const float* s_w, void* y_bf16, int64_t M,
+                                               int64_t N, int64_t K, void* stream);
+
 /* Workspace bytes fp8_linear needs for an [M, K] x [N, K]^T layer:
  * round_up(M*K, 256) + round_up(4*M, 256).  0 for invalid sizes. */
 FP8_API size_t fp8_linear_workspace_size(int64_t M, int64_t N, int64_t K);
