@@ -187,9 +187,10 @@ fp8_status_t fp8_scaled_gemm(const uint8_t* xq, const float* s_tok, const uint8_
     if (st != FP8_OK || M == 0 || N == 0) return st;
     DeviceState* d = nullptr;
     if ((st = current_device(&d)) != FP8_OK) return st;
-    // Not a programmatic dependent: the previous kernel on the stream may be
-    // the one writing wq, and the weight stream starts before the wait.
-    return run_gemm(xq, s_tok, wq, s_w, y_bf16, M, N, K, false, stream, d);
+    // A programmatic dependent of the previous kernel on the stream: before
+    // its griddepcontrol.wait a GEMM only prefetches weights into L2 (the
+    // point of coherence), so an early start cannot read stale inputs.
+    return run_gemm(xq, s_tok, wq, s_w, y_bf16, M, N, K, true, stream, d);
 }
 
 size_t fp8_linear_workspace_size(int64_t M, int64_t N, int64_t K) {
@@ -226,9 +227,9 @@ fp8_status_t fp8_linear(const void* x_bf16, const uint8_t* wq, const float* s_w,
     cudaError_t e = fp8k::launch_quant_rows(x_bf16, M, K, K, xq, K, s_tok,
                                             static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return FP8_ERR_CUDA;
-    // The GEMM is a programmatic dependent of the quantizer just launched:
-    // that kernel starts only after all earlier work on the stream is done,
-    // and it writes only xq / s_tok, which the GEMM reads after its wait.
+    // Both launches are programmatic dependents of their predecessor: each
+    // kernel waits (griddepcontrol.wait) before reading or writing memory, and
+    // the GEMM only prefetches weights into L2 before its wait.
     return run_gemm(xq, s_tok, wq, s_w, y_bf16, M, N, K, true, stream, d);
 }
 

@@ -11,15 +11,17 @@
 //     tokens (padded to MT = 16/32/64 with TMA zero fill) the narrow N side,
 //     so D^T[n, m] accumulates in TMEM (128 lanes x MT columns);
 //   * split-K over a thread-block cluster of S CTAs (one cluster per 128-row
-//     weight slab), sized so that the grid fills every SM with two CTAs;
-//   * each CTA streams its K slice of W through a deep TMA ring; the X tile of
-//     the same K slice rides along in the same stage;
+//     weight slab), sized so that the grid fills every SM with kCtasPerSm
+//     CTAs: several small CTAs per SM keep more independent TMA producers in
+//     flight than one deep ring (measured on GB300);
+//   * each CTA streams its K slice of W through a TMA ring; the X tile of the
+//     same K slice rides along in the same stage;
 //   * the S partial D^T tiles are summed through distributed shared memory in
 //     fixed rank order (deterministic), then scaled and stored as bf16 by
 //     all CTAs of the cluster, each owning 128/S rows.
-// When launched as a programmatic dependent of the quantizer, the first
-// weight tiles are requested before griddepcontrol.wait, the activations
-// after it.
+// Under programmatic dependent launch the kernel only prefetches its first
+// weight tiles into L2 before griddepcontrol.wait; every shared-memory load
+// comes after it, so an early start cannot observe stale inputs.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -38,13 +40,20 @@ constexpr int KSTEP = 32;
 constexpr int kThreads = 192;
 constexpr uint32_t W_TILE = BNW * BK;
 constexpr int kMaxSplits = 8;
+// CTAs per SM the shared-memory footprint is sized for.  Several small CTAs
+// per SM keep more independent TMA producers busy than one deep ring does.
+constexpr int kCtasPerSm = 3;
+constexpr uint32_t kSmemPerSm = 228 * 1024;
+constexpr uint32_t kCtaSmem = kSmemPerSm / kCtasPerSm - 1024;  // 1 KB reserved per CTA
+constexpr int kWBoxRows = 128;         // weight tile fetched as BNW / kWBoxRows boxes
+constexpr int kL2PrefetchBlocks = 8;   // k-blocks of W prefetched into L2 before the wait
 
 template <int MT>
 struct Cfg {
     static constexpr uint32_t X_TILE = MT * BK;
     static constexpr uint32_t STAGE_BYTES = W_TILE + X_TILE;
-    // about 108 KB of ring per CTA so that two CTAs share an SM
-    static constexpr int STAGES = (108 * 1024) / STAGE_BYTES;
+    static constexpr int STAGES = (kCtaSmem - 1024 - 512) / STAGE_BYTES;
+    static_assert(STAGES >= 2, "ring depth");
     static constexpr uint32_t RING = STAGES * STAGE_BYTES;
     static constexpr uint32_t RED_BYTES = MT * BNW * 4;  // fp32 partial D^T, aliases the ring
     static_assert(RED_BYTES <= RING, "partial tile must fit in the ring");
@@ -127,6 +136,9 @@ __global__ void __launch_bounds__(kThreads)
         tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
         tmem_relinquish();
     }
+    // the next kernel on the stream may start its prologue now (it waits for
+    // this grid's completion before touching memory)
+    pdl_launch_dependents();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -136,32 +148,27 @@ __global__ void __launch_bounds__(kThreads)
     // Role loops run on whole warps (lane 0 issues, waits warp-uniform).
     if (warp == 0) {
         // ---- TMA producer ----
-        const uint64_t w_policy = policy_evict_first();
-        // weights do not depend on the previous kernel: start streaming them
-        const int pre = nkb < C::STAGES ? nkb : C::STAGES;
+        // Before the wait, only prefetch this CTA's first weight tiles into L2
+        // (the point of coherence): nothing stale can reach shared memory even
+        // if the previous kernel is still writing the weights.
         if (lane == 0) {
-            for (int i = 0; i < pre; ++i) {
-                mbar_arrive_expect_tx(&bars->full[i], C::STAGE_BYTES);
-                tma_load_2d_hint(ring + i * C::STAGE_BYTES, &tmW, &bars->full[i], (kb0 + i) * BK,
-                                 n_blk * BNW, w_policy);
-            }
+            const int pf = nkb < kL2PrefetchBlocks ? nkb : kL2PrefetchBlocks;
+            for (int i = 0; i < pf; ++i)
+                for (int b = 0; b < BNW / kWBoxRows; ++b)
+                    tma_prefetch_l2_2d(&tmW, (kb0 + i) * BK, n_blk * BNW + b * kWBoxRows);
         }
         __syncwarp();
         pdl_wait_primary();
-        if (lane == 0) {
-            for (int i = 0; i < pre; ++i)
-                tma_load_2d(ring + i * C::STAGE_BYTES + W_TILE, &tmX, &bars->full[i],
-                            (kb0 + i) * BK, 0);
-        }
-        __syncwarp();
-        uint32_t stage = pre % C::STAGES, phase = pre == C::STAGES ? 1u : 0u;
-        for (int i = pre; i < nkb; ++i) {
+        const uint64_t w_policy = policy_evict_first();
+        uint32_t stage = 0, phase = 0;
+        for (int i = 0; i < nkb; ++i) {
             if (!warp_wait(&bars->empty[stage], phase ^ 1u, abort_flag, status)) break;
             if (lane == 0) {
                 uint8_t* st = ring + stage * C::STAGE_BYTES;
                 mbar_arrive_expect_tx(&bars->full[stage], C::STAGE_BYTES);
-                tma_load_2d_hint(st, &tmW, &bars->full[stage], (kb0 + i) * BK, n_blk * BNW,
-                                 w_policy);
+                for (int b = 0; b < BNW / kWBoxRows; ++b)
+                    tma_load_2d_hint(st + b * kWBoxRows * BK, &tmW, &bars->full[stage],
+                                     (kb0 + i) * BK, n_blk * BNW + b * kWBoxRows, w_policy);
                 tma_load_2d(st + W_TILE, &tmX, &bars->full[stage], (kb0 + i) * BK, 0);
             }
             __syncwarp();
@@ -259,10 +266,10 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-// Split count: as many clusters x splits as fill the GPU with two CTAs per SM
-// in whole waves, at least 2 k-blocks per split, at most kMaxSplits.
+// Split count: as many clusters x splits as fill the GPU with kCtasPerSm CTAs
+// per SM in whole waves, at least 2 k-blocks per split, at most kMaxSplits.
 int choose_splits(int n_tiles, int nk, int num_sms) {
-    const int slots = 2 * num_sms;
+    const int slots = kCtasPerSm * num_sms;
     int best = 1;
     double best_eff = -1.0;
     for (int s = 1; s <= kMaxSplits; ++s) {
@@ -281,7 +288,7 @@ int choose_splits(int n_tiles, int nk, int num_sms) {
 template <int MT>
 cudaError_t launch_mt(const GemmArgs& a) {
     CUtensorMap tmW, tmX;
-    if (!encode_tmap_u8(&tmW, a.wq, a.N, a.K, a.K, BK, BNW)) return cudaErrorInvalidValue;
+    if (!encode_tmap_u8(&tmW, a.wq, a.N, a.K, a.K, BK, kWBoxRows)) return cudaErrorInvalidValue;
     if (!encode_tmap_u8(&tmX, a.xq, a.M, a.K, a.K, BK, MT)) return cudaErrorInvalidValue;
     const int n_tiles = (a.N + BNW - 1) / BNW;
     const int nk = (a.K + BK - 1) / BK;
@@ -309,6 +316,11 @@ cudaError_t launch_mt(const GemmArgs& a) {
 
 cudaError_t prepare_gemm_decode() {
     cudaError_t e;
+    for (auto* k : {gemm_decode_kernel<16>, gemm_decode_kernel<32>, gemm_decode_kernel<64>}) {
+        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+    }
     e = cudaFuncSetAttribute(gemm_decode_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem_bytes<16>()));
     if (e != cudaSuccess) return e;

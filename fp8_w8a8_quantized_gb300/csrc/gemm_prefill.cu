@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(&bars->tmem_base, TMEM_COLS);
         tmem_relinquish();
     }
+    pdl_launch_dependents();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

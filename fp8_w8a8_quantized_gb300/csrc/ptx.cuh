@@ -130,6 +130,17 @@ __device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const void* tma
         : "memory");
 }
 
+// Prefetch a 2-D tile into L2 only (no shared-memory destination, no
+// completion to wait for).  Safe to issue before griddepcontrol.wait: L2 is
+// the point of coherence, so a later write by the previous kernel simply
+// replaces the prefetched lines.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -267,6 +278,17 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 
 // Non-aligned cluster barrier: every thread of every CTA of the cluster
 // arrives (release) and waits (acquire).
+// Split form of the cluster barrier: every thread of the cluster arrives,
+// and a thread's wait returns once all have arrived.  Each thread alternates
+// arrive and wait.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
@@ -276,6 +298,58 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
+}
+
+// Arrive (release at cluster scope) on an mbarrier that may live in another
+// CTA of the cluster; `cluster_addr` comes from map_to_rank.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Warp-uniform bounded wait with acquire at cluster scope (for barriers that
+// peers in the cluster arrive on); same give-up rules as wait_bounded.
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort_flag, unsigned* status) {
+    int ok = 1;
+    if ((threadIdx.x & 31u) == 0) {
+        if (!mbar_try_wait_cluster(bar, parity)) {
+            const uint64_t t0 = globaltimer_ns();
+            for (uint32_t it = 1;; ++it) {
+                if (mbar_try_wait_cluster(bar, parity)) break;
+                if (*abort_flag) {
+                    ok = 0;
+                    break;
+                }
+                if ((it & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+                    *abort_flag = 1;
+                    atomicOr(status, kErrWaitTimeout);
+                    ok = 0;
+                    break;
+                }
+            }
+        }
+    }
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    // the warp barrier orders lane 0's acquire before every lane's later reads
+    __syncwarp();
+    return ok != 0;
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");
 }
 
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {

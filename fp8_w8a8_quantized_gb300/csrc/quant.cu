@@ -107,7 +107,10 @@ __global__ void __launch_bounds__(G > kBlock ? G : kBlock)
     constexpr int B = G > kBlock ? G : kBlock;
     constexpr int ROWS = B / G;
     __shared__ float red[B / 32];
+    // launched as a programmatic dependent: start the next kernel's prologue,
+    // then wait for the previous kernel before touching memory
     pdl_launch_dependents();
+    pdl_wait_primary();
 
     const int64_t row = static_cast<int64_t>(blockIdx.x) * ROWS + threadIdx.x / G;
     const int t = threadIdx.x % G;
@@ -149,6 +152,7 @@ __global__ void __launch_bounds__(1024)
                       uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s) {
     __shared__ float red[32];
     pdl_launch_dependents();
+    pdl_wait_primary();
     const int64_t row = blockIdx.x;
     const int64_t C = K >> 4;
     const uint4* xr = reinterpret_cast<const uint4*>(x + row * ldx);
@@ -170,8 +174,29 @@ __global__ void __launch_bounds__(1024)
 
 // K == 0: an empty row has amax 0, so its scale is 1.
 __global__ void fill_ones(float* s, int64_t R) {
+    pdl_launch_dependents();
+    pdl_wait_primary();
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i < R) s[i] = 1.0f;
+}
+
+// Every kernel here waits (griddepcontrol.wait) before reading or writing
+// global memory, so it is always launched as a programmatic dependent of the
+// previous kernel on the stream: its launch overlaps that kernel's tail.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), int64_t grid, int block, cudaStream_t st,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 template <int G>
@@ -180,8 +205,7 @@ cudaError_t launch_regs(const uint16_t* x, int64_t R, int64_t K, int64_t ldx, ui
     constexpr int B = G > kBlock ? G : kBlock;
     constexpr int ROWS = B / G;
     const int64_t grid = (R + ROWS - 1) / ROWS;
-    quant_rows_regs<G><<<static_cast<unsigned>(grid), B, 0, st>>>(x, R, K, ldx, q, ldq, s);
-    return cudaGetLastError();
+    return launch_pdl(quant_rows_regs<G>, grid, B, st, x, R, K, ldx, q, ldq, s);
 }
 
 }  // namespace
@@ -191,10 +215,7 @@ cudaError_t launch_regs(const uint16_t* x, int64_t R, int64_t K, int64_t ldx, ui
 cudaError_t launch_quant_rows(const void* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q,
                               int64_t ldq, float* s, cudaStream_t st) {
     const uint16_t* xb = static_cast<const uint16_t*>(x);
-    if (K == 0) {
-        fill_ones<<<static_cast<unsigned>((R + 255) / 256), 256, 0, st>>>(s, R);
-        return cudaGetLastError();
-    }
+    if (K == 0) return launch_pdl(fill_ones, (R + 255) / 256, 256, st, s, R);
     const int64_t C = K / 16;
     if (C <= 32 * kVPT) return launch_regs<32>(xb, R, K, ldx, q, ldq, s, st);
     if (C <= 64 * kVPT) return launch_regs<64>(xb, R, K, ldx, q, ldq, s, st);
@@ -202,8 +223,7 @@ cudaError_t launch_quant_rows(const void* x, int64_t R, int64_t K, int64_t ldx, 
     if (C <= 256 * kVPT) return launch_regs<256>(xb, R, K, ldx, q, ldq, s, st);
     if (C <= 512 * kVPT) return launch_regs<512>(xb, R, K, ldx, q, ldq, s, st);
     if (C <= 1024 * kVPT) return launch_regs<1024>(xb, R, K, ldx, q, ldq, s, st);
-    quant_rows_stream<<<static_cast<unsigned>(R), 1024, 0, st>>>(xb, R, K, ldx, q, ldq, s);
-    return cudaGetLastError();
+    return launch_pdl(quant_rows_stream, R, 1024, st, xb, R, K, ldx, q, ldq, s);
 }
 
 }  // namespace fp8k
