@@ -126,7 +126,7 @@ fp8_status_t check_gemm(const uint8_t* xq, const float* s_tok, const uint8_t* wq
 }
 
 fp8_status_t run_gemm(const uint8_t* xq, const float* s_tok, const uint8_t* wq, const float* s_w,
-                      void* y, int64_t M, int64_t N, int64_t K, bool pdl, void* stream,
+                      void* y, int64_t M, int64_t N, int64_t K, bool after_quant, void* stream,
                       DeviceState* d) {
     fp8k::GemmArgs a;
     a.xq = xq;
@@ -139,7 +139,8 @@ fp8_status_t run_gemm(const uint8_t* xq, const float* s_tok, const uint8_t* wq, 
     a.K = static_cast<int>(K);
     a.status = d->status;
     a.num_sms = d->num_sms;
-    a.pdl = pdl;
+    a.pdl = true;
+    a.w_early = after_quant;
     a.stream = static_cast<cudaStream_t>(stream);
     cudaError_t e = M <= fp8k::kDecodeMaxM ? fp8k::launch_gemm_decode(a)
                                            : fp8k::launch_gemm_prefill(a);
@@ -187,10 +188,11 @@ fp8_status_t fp8_scaled_gemm(const uint8_t* xq, const float* s_tok, const uint8_
     if (st != FP8_OK || M == 0 || N == 0) return st;
     DeviceState* d = nullptr;
     if ((st = current_device(&d)) != FP8_OK) return st;
-    // A programmatic dependent of the previous kernel on the stream: before
-    // its griddepcontrol.wait a GEMM only prefetches weights into L2 (the
-    // point of coherence), so an early start cannot read stale inputs.
-    return run_gemm(xq, s_tok, wq, s_w, y_bf16, M, N, K, true, stream, d);
+    // A programmatic dependent of the previous kernel on the stream, which may
+    // be anything (even the kernel writing wq): before its griddepcontrol.wait
+    // the GEMM only prefetches weights into L2, the point of coherence, so an
+    // early start cannot read stale inputs.
+    return run_gemm(xq, s_tok, wq, s_w, y_bf16, M, N, K, false, stream, d);
 }
 
 size_t fp8_linear_workspace_size(int64_t M, int64_t N, int64_t K) {
@@ -227,9 +229,11 @@ fp8_status_t fp8_linear(const void* x_bf16, const uint8_t* wq, const float* s_w,
     cudaError_t e = fp8k::launch_quant_rows(x_bf16, M, K, K, xq, K, s_tok,
                                             static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return FP8_ERR_CUDA;
-    // Both launches are programmatic dependents of their predecessor: each
-    // kernel waits (griddepcontrol.wait) before reading or writing memory, and
-    // the GEMM only prefetches weights into L2 before its wait.
+    // Both launches are programmatic dependents of their predecessor.  The
+    // quantizer waits before touching memory and releases the GEMM only after
+    // that wait, so every earlier kernel (any writer of wq) has finished when
+    // the GEMM starts: it may stream weights before its own wait, and reads
+    // the quantized activations after it.
     return run_gemm(xq, s_tok, wq, s_w, y_bf16, M, N, K, true, stream, d);
 }
 

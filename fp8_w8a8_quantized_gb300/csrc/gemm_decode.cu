@@ -19,9 +19,11 @@
 //   * the S partial D^T tiles are summed through distributed shared memory in
 //     fixed rank order (deterministic), then scaled and stored as bf16 by
 //     all CTAs of the cluster, each owning 128/S rows.
-// Under programmatic dependent launch the kernel only prefetches its first
-// weight tiles into L2 before griddepcontrol.wait; every shared-memory load
-// comes after it, so an early start cannot observe stale inputs.
+// Under programmatic dependent launch, what the kernel reads before
+// griddepcontrol.wait depends on its predecessor: after the library's own
+// quantizer (which releases it only once every earlier kernel has finished)
+// it fills its ring with weights at once; otherwise it only prefetches the
+// first weight tiles into L2, so an early start cannot observe stale inputs.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -29,24 +31,14 @@
 #include <cstdint>
 
 #include "launch.h"
+#include "decode_common.cuh"
 #include "ptx.cuh"
 
 namespace fp8k {
 namespace {
 
-constexpr int BNW = 128;  // weight rows per CTA (MMA M)
-constexpr int BK = 128;   // bytes of K per stage
-constexpr int KSTEP = 32;
-constexpr int kThreads = 192;
-constexpr uint32_t W_TILE = BNW * BK;
-constexpr int kMaxSplits = 8;
-// CTAs per SM the shared-memory footprint is sized for.  Several small CTAs
-// per SM keep more independent TMA producers busy than one deep ring does.
-constexpr int kCtasPerSm = 3;
-constexpr uint32_t kSmemPerSm = 228 * 1024;
-constexpr uint32_t kCtaSmem = kSmemPerSm / kCtasPerSm - 1024;  // 1 KB reserved per CTA
-constexpr int kWBoxRows = 128;         // weight tile fetched as BNW / kWBoxRows boxes
-constexpr int kL2PrefetchBlocks = 8;   // k-blocks of W prefetched into L2 before the wait
+using namespace decode;
+constexpr int kWBoxRows = 128;  // weight tile fetched as BNW / kWBoxRows boxes
 
 template <int MT>
 struct Cfg {
@@ -76,31 +68,11 @@ constexpr size_t smem_bytes() {
 }
 
 template <int MT>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float* out) {
-    if constexpr (MT == 16) {
-        uint32_t r[16];
-        tmem_ld_32x32b_x16(taddr, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) out[j] = __uint_as_float(r[j]);
-    } else {
-#pragma unroll
-        for (int h = 0; h < MT / 32; ++h) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(taddr + h * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) out[h * 32 + j] = __uint_as_float(r[j]);
-        }
-    }
-}
-
-template <int MT>
 __global__ void __launch_bounds__(kThreads)
     gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW,
                        const __grid_constant__ CUtensorMap tmX, const float* __restrict__ s_tok,
                        const float* __restrict__ s_w, __nv_bfloat16* __restrict__ y, int M, int N,
-                       int K, int splits, unsigned* status) {
+                       int K, int splits, int w_early, unsigned* status) {
     using C = Cfg<MT>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -148,20 +120,38 @@ __global__ void __launch_bounds__(kThreads)
     // Role loops run on whole warps (lane 0 issues, waits warp-uniform).
     if (warp == 0) {
         // ---- TMA producer ----
-        // Before the wait, only prefetch this CTA's first weight tiles into L2
-        // (the point of coherence): nothing stale can reach shared memory even
-        // if the previous kernel is still writing the weights.
+        const uint64_t w_policy = policy_evict_first();
+        // Weights before the wait: when this launch follows the library's own
+        // quantizer (w_early), every earlier kernel has finished, so the first
+        // stages are filled with weights at once.  Otherwise only prefetch the
+        // first weight tiles into L2 (the point of coherence): nothing stale can
+        // reach shared memory even if the previous kernel still writes them.
+        const int pre = w_early ? (nkb < C::STAGES ? nkb : C::STAGES) : 0;
         if (lane == 0) {
-            const int pf = nkb < kL2PrefetchBlocks ? nkb : kL2PrefetchBlocks;
-            for (int i = 0; i < pf; ++i)
-                for (int b = 0; b < BNW / kWBoxRows; ++b)
-                    tma_prefetch_l2_2d(&tmW, (kb0 + i) * BK, n_blk * BNW + b * kWBoxRows);
+            if (w_early) {
+                for (int i = 0; i < pre; ++i) {
+                    mbar_arrive_expect_tx(&bars->full[i], C::STAGE_BYTES);
+                    for (int b = 0; b < BNW / kWBoxRows; ++b)
+                        tma_load_2d_hint(ring + i * C::STAGE_BYTES + b * kWBoxRows * BK, &tmW,
+                                         &bars->full[i], (kb0 + i) * BK,
+                                         n_blk * BNW + b * kWBoxRows, w_policy);
+                }
+            } else {
+                const int pf = nkb < kL2PrefetchBlocks ? nkb : kL2PrefetchBlocks;
+                for (int i = 0; i < pf; ++i)
+                    for (int b = 0; b < BNW / kWBoxRows; ++b)
+                        tma_prefetch_l2_2d(&tmW, (kb0 + i) * BK, n_blk * BNW + b * kWBoxRows);
+            }
         }
         __syncwarp();
         pdl_wait_primary();
-        const uint64_t w_policy = policy_evict_first();
-        uint32_t stage = 0, phase = 0;
-        for (int i = 0; i < nkb; ++i) {
+        if (lane == 0)
+            for (int i = 0; i < pre; ++i)
+                tma_load_2d(ring + i * C::STAGE_BYTES + W_TILE, &tmX, &bars->full[i],
+                            (kb0 + i) * BK, 0);
+        __syncwarp();
+        uint32_t stage = pre % C::STAGES, phase = pre == C::STAGES ? 1u : 0u;
+        for (int i = pre; i < nkb; ++i) {
             if (!warp_wait(&bars->empty[stage], phase ^ 1u, abort_flag, status)) break;
             if (lane == 0) {
                 uint8_t* st = ring + stage * C::STAGE_BYTES;
@@ -266,25 +256,6 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-// Split count: as many clusters x splits as fill the GPU with kCtasPerSm CTAs
-// per SM in whole waves, at least 2 k-blocks per split, at most kMaxSplits.
-int choose_splits(int n_tiles, int nk, int num_sms) {
-    const int slots = kCtasPerSm * num_sms;
-    int best = 1;
-    double best_eff = -1.0;
-    for (int s = 1; s <= kMaxSplits; ++s) {
-        if (s > 1 && nk < 2 * s) break;
-        const int ctas = n_tiles * s;
-        const int waves = (ctas + slots - 1) / slots;
-        const double eff = static_cast<double>(ctas) / (static_cast<double>(waves) * slots);
-        if (eff > best_eff + 0.02) {
-            best_eff = eff;
-            best = s;
-        }
-    }
-    return best;
-}
-
 template <int MT>
 cudaError_t launch_mt(const GemmArgs& a) {
     CUtensorMap tmW, tmX;
@@ -309,7 +280,8 @@ cudaError_t launch_mt(const GemmArgs& a) {
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, gemm_decode_kernel<MT>, tmW, tmX, a.s_tok, a.s_w,
-                              static_cast<__nv_bfloat16*>(a.y), a.M, a.N, a.K, splits, a.status);
+                              static_cast<__nv_bfloat16*>(a.y), a.M, a.N, a.K, splits,
+                              a.w_early ? 1 : 0, a.status);
 }
 
 }  // namespace

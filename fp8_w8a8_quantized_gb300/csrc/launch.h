@@ -25,6 +25,11 @@ struct GemmArgs {
     unsigned* status;     // device status word
     int num_sms;
     bool pdl;             // launch as a programmatic dependent of the previous kernel
+    // The previous kernel is this library's quantizer, which releases its
+    // dependents only after every earlier kernel has finished: the weights are
+    // final, so the decode GEMM may load them into shared memory before its
+    // griddepcontrol.wait (only the activations must wait).
+    bool w_early;
     cudaStream_t stream;
 };
 

@@ -27,47 +27,13 @@
 #include <cstdint>
 
 #include "ptx.cuh"
+#include "quant_math.cuh"
 
 namespace fp8k {
 namespace {
 
 constexpr int kBlock = 256;  // threads per CTA for G <= 256
 constexpr int kVPT = 4;      // 16-element chunks per thread (register path)
-
-__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
-
-__device__ __forceinline__ float amax8(const uint4& v, float m) {
-    m = fmaxf(m, fabsf(bf16lo(v.x)));
-    m = fmaxf(m, fabsf(bf16hi(v.x)));
-    m = fmaxf(m, fabsf(bf16lo(v.y)));
-    m = fmaxf(m, fabsf(bf16hi(v.y)));
-    m = fmaxf(m, fabsf(bf16lo(v.z)));
-    m = fmaxf(m, fabsf(bf16hi(v.z)));
-    m = fmaxf(m, fabsf(bf16lo(v.w)));
-    m = fmaxf(m, fabsf(bf16hi(v.w)));
-    return m;
-}
-
-// Two fp32 values -> two E4M3 codes (RN, saturating to +-448); `lo` lands in
-// the low byte (lower address).
-__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-// Four bf16 pairs (8 values) -> 8 codes packed in two 32-bit words.
-__device__ __forceinline__ uint2 quant8(const uint4& v, float s) {
-    uint2 o;
-    const uint32_t a = cvt_e4m3x2(__fdiv_rn(bf16lo(v.x), s), __fdiv_rn(bf16hi(v.x), s));
-    const uint32_t b = cvt_e4m3x2(__fdiv_rn(bf16lo(v.y), s), __fdiv_rn(bf16hi(v.y), s));
-    const uint32_t c = cvt_e4m3x2(__fdiv_rn(bf16lo(v.z), s), __fdiv_rn(bf16hi(v.z), s));
-    const uint32_t d = cvt_e4m3x2(__fdiv_rn(bf16lo(v.w), s), __fdiv_rn(bf16hi(v.w), s));
-    o.x = a | (b << 16);
-    o.y = c | (d << 16);
-    return o;
-}
 
 // Read-once 16-byte load that does not allocate in L1.
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
@@ -76,10 +42,6 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;
-}
-
-__device__ __forceinline__ float scale_of(float amax) {
-    return amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
 }
 
 // Max over the G threads of a row group.  `red` holds one float per warp.
@@ -107,10 +69,12 @@ __global__ void __launch_bounds__(G > kBlock ? G : kBlock)
     constexpr int B = G > kBlock ? G : kBlock;
     constexpr int ROWS = B / G;
     __shared__ float red[B / 32];
-    // launched as a programmatic dependent: start the next kernel's prologue,
-    // then wait for the previous kernel before touching memory
-    pdl_launch_dependents();
+    // Launched as a programmatic dependent: wait for the previous kernel
+    // before touching memory, and only then let the next kernel start -- so
+    // when a dependent GEMM starts, every kernel before this one has finished
+    // (it may then read the weights before its own wait).
     pdl_wait_primary();
+    pdl_launch_dependents();
 
     const int64_t row = static_cast<int64_t>(blockIdx.x) * ROWS + threadIdx.x / G;
     const int t = threadIdx.x % G;
@@ -151,8 +115,8 @@ __global__ void __launch_bounds__(1024)
     quant_rows_stream(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx,
                       uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s) {
     __shared__ float red[32];
-    pdl_launch_dependents();
     pdl_wait_primary();
+    pdl_launch_dependents();
     const int64_t row = blockIdx.x;
     const int64_t C = K >> 4;
     const uint4* xr = reinterpret_cast<const uint4*>(x + row * ldx);
@@ -174,15 +138,16 @@ __global__ void __launch_bounds__(1024)
 
 // K == 0: an empty row has amax 0, so its scale is 1.
 __global__ void fill_ones(float* s, int64_t R) {
-    pdl_launch_dependents();
     pdl_wait_primary();
+    pdl_launch_dependents();
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i < R) s[i] = 1.0f;
 }
 
 // Every kernel here waits (griddepcontrol.wait) before reading or writing
 // global memory, so it is always launched as a programmatic dependent of the
-// previous kernel on the stream: its launch overlaps that kernel's tail.
+// previous kernel on the stream: its launch overlaps that kernel's tail.  It
+// releases its own dependents only after that wait.
 template <typename... Params, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(Params...), int64_t grid, int block, cudaStream_t st,
                        Args... args) {
