@@ -60,6 +60,7 @@ struct Bars {
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
+    float s_tok[64];  // token scales, staged once for the reduction
 };
 
 template <int MT>
@@ -219,28 +220,46 @@ __global__ void __launch_bounds__(kThreads)
         // consumed by an MMA that has finished): reuse it for the partial.
 #pragma unroll
         for (int j = 0; j < MT; ++j) red[j * BNW + nl] = v[j];
+        if (warp == 2)
+            for (int m = lane; m < M; m += 32) bars->s_tok[m] = __ldg(s_tok + m);
     }
 
     // All partials of the cluster are in shared memory after this barrier.
     cluster_sync_all();
 
     {
+        // This CTA owns weight rows [lo, hi) of the slab.  Each thread keeps
+        // one row (its weight scale in a register, its peers' partial
+        // addresses mapped once) and walks tokens m = g, g + groups, ...; the
+        // S partial loads of an output are independent, issued together and
+        // summed in rank order (deterministic).
         const int rows_per = (BNW + splits - 1) / splits;
         const int lo = static_cast<int>(rank) * rows_per;
         const int hi = min(BNW, lo + rows_per);
         const int width = hi - lo;
-        const int total = width > 0 ? width * M : 0;
-        const uint32_t red_addr = smem_u32(red);
-        for (int e = threadIdx.x; e < total; e += kThreads) {
-            const int m = e / width;
-            const int nl = lo + (e - m * width);
-            const int n = n_blk * BNW + nl;
-            const uint32_t off = static_cast<uint32_t>((m * BNW + nl) * 4);
-            float acc = 0.0f;
-            for (int j = 0; j < splits; ++j) acc += ld_dsmem_f32(map_to_rank(red_addr + off, j));
-            if (n < N) {
-                const float out = (acc * __ldg(s_tok + m)) * __ldg(s_w + n);
-                y[static_cast<int64_t>(m) * N + n] = __float2bfloat16_rn(out);
+        const int groups = width > 0 ? kThreads / width : 0;
+        if (groups > 0 && static_cast<int>(threadIdx.x) < groups * width) {
+            const int r = lo + static_cast<int>(threadIdx.x) % width;
+            const int n = n_blk * BNW + r;
+            const float sw = n < N ? __ldg(s_w + n) : 0.0f;
+            const uint32_t base = smem_u32(red) + static_cast<uint32_t>(r * 4);
+            uint32_t peer[kMaxSplits];
+#pragma unroll
+            for (int j = 0; j < kMaxSplits; ++j) peer[j] = j < splits ? map_to_rank(base, j) : 0u;
+#pragma unroll 4
+            for (int m = static_cast<int>(threadIdx.x) / width; m < M; m += groups) {
+                const uint32_t off = static_cast<uint32_t>(m * BNW * 4);
+                float part[kMaxSplits];
+#pragma unroll
+                for (int j = 0; j < kMaxSplits; ++j)
+                    part[j] = j < splits ? ld_dsmem_f32(peer[j] + off) : 0.0f;
+                float acc = 0.0f;
+#pragma unroll
+                for (int j = 0; j < kMaxSplits; ++j)
+                    if (j < splits) acc += part[j];
+                if (n < N)
+                    y[static_cast<int64_t>(m) * N + n] =
+                        __float2bfloat16_rn((acc * bars->s_tok[m]) * sw);
             }
         }
     }
