@@ -87,6 +87,12 @@ def _load():
         lib.orc_linear_points.restype = None
         lib.orc_linear_points.argtypes = [_vp, _i64, _vp, _vp, _i64, _vp, _i64,
                                           _i64, _vp, _vp, _vp]
+        lib.orc_quant_rows_scaled_bf16.restype = None
+        lib.orc_quant_rows_scaled_bf16.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _i64]
+        lib.orc_quant_tensor_bf16.restype = None
+        lib.orc_quant_tensor_bf16.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp]
+        lib.orc_kv_cache_quant_bf16.restype = None
+        lib.orc_kv_cache_quant_bf16.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp]
         lib.orc_num_threads.restype = ctypes.c_int
         lib.orc_num_threads.argtypes = []
         _lib = lib
@@ -169,6 +175,49 @@ def quant_rows_f32(x: np.ndarray):
     if R:
         lib.orc_quant_rows_f32(_ptr(xf), R, K, K, _ptr(q), K, _ptr(s))
     return q, s
+
+
+def quant_rows_scaled_bf16(x_bits: np.ndarray, scales) -> np.ndarray:
+    """Each row r quantized with the given scale s[r] (a static scale is the
+    same value for every row): q = E4M3(fl32(x / s))."""
+    lib = _load()
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    R, K = x.shape
+    s = np.ascontiguousarray(np.broadcast_to(np.asarray(scales, dtype=np.float32), (R,)))
+    q = np.empty((R, K), dtype=np.uint8)
+    if R and K:
+        lib.orc_quant_rows_scaled_bf16(_ptr(x), R, K, K, _ptr(s), _ptr(q), K)
+    return q
+
+
+def quant_tensor_bf16(x_bits: np.ndarray):
+    """Dynamic per-tensor quantization: one scale amax(all)/448 (1 if all
+    zero).  Returns (codes, scale as fp32 scalar)."""
+    lib = _load()
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    R, K = x.shape
+    q = np.empty((R, K), dtype=np.uint8)
+    s = np.ones((1,), dtype=np.float32)
+    if R and K:
+        lib.orc_quant_tensor_bf16(_ptr(x), R, K, K, _ptr(q), K, _ptr(s))
+    return q, s[0]
+
+
+def kv_cache_quant_bf16(x_bits: np.ndarray, scale, slots, n_slots: int) -> np.ndarray:
+    """KV-cache write: x [T, H, D] bf16 bits, scale [H] (per head) or a
+    scalar (per tensor), slots [T] (negative = skip) or None (identity).
+    Returns the cache [n_slots, H, D] of E4M3 codes (untouched rows 0)."""
+    lib = _load()
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    T, H, D = x.shape
+    sc = np.atleast_1d(np.asarray(scale, dtype=np.float32))
+    stride = 1 if sc.size == H and H > 1 else 0
+    sl = None if slots is None else np.ascontiguousarray(slots, dtype=np.int64)
+    cache = np.zeros((n_slots, H, D), dtype=np.uint8)
+    if T and H and D:
+        lib.orc_kv_cache_quant_bf16(_ptr(x), T, H, D, _ptr(sc), stride,
+                                    None if sl is None else _ptr(sl), _ptr(cache))
+    return cache
 
 
 # --------------------------------------------------------------------------

@@ -283,3 +283,74 @@ int orc_num_threads(void)
     return 1;
 #endif
 }
+
+/* ------------------------------------------------------------------------ */
+/* Per-tensor and static scales; KV-cache quantize-on-write                 */
+/* ------------------------------------------------------------------------ */
+
+/* Rows quantized with a given scale each: q[r,k] = E4M3(fl32(x[r,k] / s[r])).
+ * A static (calibrated) scale is the same s for every row ("Quantization:
+ * FP8 inference and KV-cache quantization", "Dynamic scales or static
+ * scales": values beyond 448 s clamp to 448 in saturating mode). */
+void orc_quant_rows_scaled_bf16(const uint16_t* x, int64_t R, int64_t K, int64_t ldx,
+                                const float* s, uint8_t* q, int64_t ldq)
+{
+    int64_t r;
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < R; ++r) {
+        int64_t k;
+        for (k = 0; k < K; ++k) {
+            volatile float t = bf16_to_f32(x[r * ldx + k]) / s[r];
+            q[r * ldq + k] = orc_e4m3_encode((double)t);
+        }
+    }
+}
+
+/* Dynamic per-tensor scale ("FP8 Quantization", "Choose Scaling Strategy"
+ * and "Granularity": one scale for the whole tensor, from its max |x|,
+ * computed at run time): s = fl32(amax / 448) over all R x K values (1 if
+ * all are zero), then every value divided by s. */
+void orc_quant_tensor_bf16(const uint16_t* x, int64_t R, int64_t K, int64_t ldx,
+                           uint8_t* q, int64_t ldq, float* s_out)
+{
+    float amax = 0.0f, s;
+    int64_t r, k;
+    for (r = 0; r < R; ++r)
+        for (k = 0; k < K; ++k) {
+            float a = fabsf(bf16_to_f32(x[r * ldx + k]));
+            if (a > amax)
+                amax = a;
+        }
+    s = (amax > 0.0f) ? amax / 448.0f : 1.0f;
+    for (r = 0; r < R; ++r)
+        for (k = 0; k < K; ++k) {
+            volatile float t = bf16_to_f32(x[r * ldx + k]) / s;
+            q[r * ldq + k] = orc_e4m3_encode((double)t);
+        }
+    *s_out = s;
+}
+
+/* FP8 KV-cache write ("Quantization: FP8 inference and KV-cache
+ * quantization", "Turning it on in an engine": one scale per tensor or per
+ * attention head, 1.0 when uncalibrated; values beyond 448 are clipped).
+ * x is [T, H, D] bf16; scale has H entries (per head) or 1 (per tensor,
+ * scale_stride 0); token t goes to cache row slot[t] (skipped if negative);
+ * cache is [slots, H, D] E4M3. */
+void orc_kv_cache_quant_bf16(const uint16_t* x, int64_t T, int64_t H, int64_t D,
+                             const float* scale, int64_t scale_stride,
+                             const int64_t* slot, uint8_t* cache)
+{
+    int64_t t;
+    for (t = 0; t < T; ++t) {
+        int64_t row = slot ? slot[t] : t, h, d;
+        if (row < 0)
+            continue;
+        for (h = 0; h < H; ++h) {
+            const float s = scale[h * scale_stride];
+            for (d = 0; d < D; ++d) {
+                volatile float v = bf16_to_f32(x[(t * H + h) * D + d]) / s;
+                cache[(row * H + h) * D + d] = orc_e4m3_encode((double)v);
+            }
+        }
+    }
+}
