@@ -92,7 +92,7 @@ def _load():
         lib.orc_quant_tensor_bf16.restype = None
         lib.orc_quant_tensor_bf16.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp]
         lib.orc_kv_cache_quant_bf16.restype = None
-        lib.orc_kv_cache_quant_bf16.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp]
+        lib.orc_kv_cache_quant_bf16.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp]
         lib.orc_num_threads.restype = ctypes.c_int
         lib.orc_num_threads.argtypes = []
         _lib = lib
@@ -205,7 +205,8 @@ def quant_tensor_bf16(x_bits: np.ndarray):
 
 def kv_cache_quant_bf16(x_bits: np.ndarray, scale, slots, n_slots: int) -> np.ndarray:
     """KV-cache write: x [T, H, D] bf16 bits, scale [H] (per head) or a
-    scalar (per tensor), slots [T] (negative = skip) or None (identity).
+    scalar (per tensor), slots [T] or None (identity); a token whose slot is
+    negative or >= n_slots is skipped.
     Returns the cache [n_slots, H, D] of E4M3 codes (untouched rows 0)."""
     lib = _load()
     x = np.ascontiguousarray(x_bits, dtype=np.uint16)
@@ -216,7 +217,7 @@ def kv_cache_quant_bf16(x_bits: np.ndarray, scale, slots, n_slots: int) -> np.nd
     cache = np.zeros((n_slots, H, D), dtype=np.uint8)
     if T and H and D:
         lib.orc_kv_cache_quant_bf16(_ptr(x), T, H, D, _ptr(sc), stride,
-                                    None if sl is None else _ptr(sl), _ptr(cache))
+                                    None if sl is None else _ptr(sl), n_slots, _ptr(cache))
     return cache
 
 

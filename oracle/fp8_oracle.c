@@ -334,16 +334,16 @@ void orc_quant_tensor_bf16(const uint16_t* x, int64_t R, int64_t K, int64_t ldx,
  * quantization", "Turning it on in an engine": one scale per tensor or per
  * attention head, 1.0 when uncalibrated; values beyond 448 are clipped).
  * x is [T, H, D] bf16; scale has H entries (per head) or 1 (per tensor,
- * scale_stride 0); token t goes to cache row slot[t] (skipped if negative);
- * cache is [slots, H, D] E4M3. */
+ * scale_stride 0); token t goes to cache row slot[t] (or t), skipped when
+ * that row is negative or not below n_slots; cache is [n_slots, H, D] E4M3. */
 void orc_kv_cache_quant_bf16(const uint16_t* x, int64_t T, int64_t H, int64_t D,
                              const float* scale, int64_t scale_stride,
-                             const int64_t* slot, uint8_t* cache)
+                             const int64_t* slot, int64_t n_slots, uint8_t* cache)
 {
     int64_t t;
     for (t = 0; t < T; ++t) {
         int64_t row = slot ? slot[t] : t, h, d;
-        if (row < 0)
+        if (row < 0 || row >= n_slots)
             continue;
         for (h = 0; h < H; ++h) {
             const float s = scale[h * scale_stride];

@@ -74,17 +74,17 @@ def test_kv_cache_scale_one_and_clipping(oracle_mod):
 
 
 def test_kv_cache_per_head_scales_and_slots(oracle_mod):
-    T, H, D = 5, 4, 64
+    T, H, D = 6, 4, 64
     g = torch.Generator().manual_seed(3)
     x = (torch.randn(T, H, D, generator=g) * 4).to(torch.bfloat16)
     scale = np.array([0.5, 1.0, 2.0, 0.125], dtype=np.float32)
-    slots = np.array([7, -1, 0, 3, 9], dtype=np.int64)
+    slots = np.array([7, -1, 0, 3, 9, 10], dtype=np.int64)  # 10 is past the cache
     cache = oracle_mod.kv_cache_quant_bf16(bits(x), scale, slots, 10)
     for t in range(T):
-        if slots[t] < 0:
+        if slots[t] < 0 or slots[t] >= 10:
             continue
         for h in range(H):
             ref = oracle_mod.quant_rows_scaled_bf16(bits(x[t, h][None]), scale[h])[0]
             assert np.array_equal(cache[slots[t], h], ref)
-    untouched = [r for r in range(10) if r not in set(slots[slots >= 0])]
+    untouched = [r for r in range(10) if r not in set(slots.tolist())]
     assert np.all(cache[untouched] == 0)
