@@ -366,6 +366,8 @@ def run_ours(args):
                "workload": "llama-3.1-8b prefill layers, M in {2048,8192}, 8 fp8_linear calls"}
     del pxs, pys, pws
 
+    variants = variant_rates(pkg, workloads, dev, stream, timed, hbm_peak, args.steps)
+
     # --- e2e: public API with pinned host buffers, copies in the timed region
     hx = [x.cpu().pin_memory() for x in xs]
     hy = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys]
@@ -413,12 +415,70 @@ def run_ours(args):
             "gpu_launches": 2 * len(calls) * args.steps,
             "roofline": roofline,
             "prefill": prefill,
+            "scale_variants": variants,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
     return 0
+
+
+def variant_rates(pkg, workloads, dev, stream, timed, hbm_peak, steps):
+    """GB/s of the quantizers with other scale granularities, each on inputs
+    rotated over buffers larger than L2 in total.  Algorithmic bytes: bf16
+    read once, E4M3 written once (plus the fp32 per-row scales / slot ids)."""
+    import torch
+
+    out = {}
+    M, K, nbuf = 8192, 4096, 4           # 8B prefill chunk entering q/k/v or gate/up
+    xs = [workloads.student_t_outliers(M, K, workloads.SEED_PREFILL + i, dev)
+          for i in range(nbuf)]
+    qs = [torch.empty((M, K), dtype=torch.uint8, device=dev) for _ in range(nbuf)]
+    s_rows = torch.empty(M, dtype=torch.float32, device=dev)
+    s_static = torch.tensor([0.05], dtype=torch.float32, device=dev)
+    s_out = torch.empty(1, dtype=torch.float32, device=dev)
+    ws = torch.empty(int(pkg.lib().fp8_quant_per_tensor_workspace_size(M, K)),
+                     dtype=torch.uint8, device=dev)
+    n = max(steps, 40)
+    act_bytes = 3 * M * K + 4 * M
+
+    def rate(seconds, nbytes):
+        gbs = nbytes * n / seconds / 1e9
+        return {"gbs": gbs, "frac": gbs / hbm_peak, "us_per_launch": seconds / n * 1e6}
+
+    t = timed(lambda i: pkg.fp8_quant_per_token(xs[i % nbuf], xq=qs[i % nbuf], s_tok=s_rows,
+                                                stream=stream), n, 3)
+    out["per_token"] = dict(rate(t, act_bytes), workload=f"{M}x{K} bf16", launches=1)
+    t = timed(lambda i: pkg.fp8_quant_static(xs[i % nbuf], s_static, xq=qs[i % nbuf],
+                                             s_rows=s_rows, stream=stream), n, 3)
+    out["static"] = dict(rate(t, act_bytes), workload=f"{M}x{K} bf16", launches=1)
+    t = timed(lambda i: pkg.fp8_quant_per_tensor(xs[i % nbuf], xq=qs[i % nbuf], s=s_out,
+                                                 s_rows=s_rows, workspace=ws, stream=stream),
+              n, 3)
+    out["per_tensor"] = dict(rate(t, act_bytes), workload=f"{M}x{K} bf16", launches=2,
+                             note="two passes over x; the second mostly hits L2")
+    del xs, qs
+
+    # KV-cache write: 8 KV heads x 128, one layer's keys (or values) of an
+    # 8192-token prefill scattered into a paged cache, 16 layers rotated
+    T, H, D, nl = 8192, 8, 128, 16
+    n_slots = T + 1024
+    kvs = [workloads.student_t_outliers(T * H, D, workloads.SEED_PREFILL + 10 + i, dev)
+           .view(T, H, D) for i in range(nl)]
+    caches = [torch.zeros((n_slots, H, D), dtype=torch.uint8, device=dev) for _ in range(nl)]
+    g = torch.Generator(device="cpu")
+    g.manual_seed(7)
+    slots = torch.randperm(n_slots, generator=g)[:T].to(torch.int64).to(dev)
+    kv_scale = torch.linspace(0.25, 2.0, H, dtype=torch.float32, device=dev)
+    t = timed(lambda i: pkg.fp8_kv_cache_quant(kvs[i % nl], kv_scale, caches[i % nl], slots,
+                                               stream=stream), n, 3)
+    out["kv_cache_write"] = dict(rate(t, 3 * T * H * D + 8 * T),
+                                 workload=f"T={T} H={H} D={D}, per-head scales, paged slots",
+                                 launches=1)
+    del kvs, caches
+    torch.cuda.synchronize()
+    return out
 
 
 # DRAM traffic of the decode GEMM relative to its algorithmic bytes, from an
@@ -437,9 +497,12 @@ def run_case(spec: str, reps: int = 4):
 
     import fp8_w8a8_quantized_gb300 as pkg
     from fp8_w8a8_quantized_gb300 import build, workloads
-    M, K, N = (int(v) for v in spec.split(","))
     build.build()
     dev = torch.device("cuda", 0)
+    kind, *dims = spec.split(",")
+    if kind in ("static", "tensor", "kv"):
+        return run_variant_case(pkg, workloads, dev, kind, [int(v) for v in dims], reps)
+    M, K, N = (int(v) for v in spec.split(","))
     w = workloads.weights(N, K, workloads.SEED_DECODE, dev)
     wq, s_w = pkg.fp8_quant_per_channel_weights(w)
     del w
@@ -457,6 +520,34 @@ def run_case(spec: str, reps: int = 4):
     return 0
 
 
+def run_variant_case(pkg, workloads, dev, kind, dims, reps):
+    """static,M,K / tensor,M,K / kv,T,H,D: one quantizer variant `reps` times."""
+    import torch
+    if kind == "kv":
+        T, H, D = dims
+        kv = workloads.student_t_outliers(T * H, D, workloads.SEED_PREFILL, dev).view(T, H, D)
+        cache = torch.zeros((T + 1024, H, D), dtype=torch.uint8, device=dev)
+        slots = torch.randperm(T + 1024)[:T].to(torch.int64).to(dev)
+        sc = torch.linspace(0.25, 2.0, H, dtype=torch.float32, device=dev)
+        run = lambda: pkg.fp8_kv_cache_quant(kv, sc, cache, slots)
+    else:
+        M, K = dims
+        x = workloads.student_t_outliers(M, K, workloads.SEED_PREFILL, dev)
+        q = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        s_rows = torch.empty(M, dtype=torch.float32, device=dev)
+        if kind == "static":
+            s = torch.tensor([0.05], dtype=torch.float32, device=dev)
+            run = lambda: pkg.fp8_quant_static(x, s, xq=q, s_rows=s_rows)
+        else:
+            run = lambda: pkg.fp8_quant_per_tensor(x, xq=q, s_rows=s_rows)
+    torch.cuda.synchronize()
+    for _ in range(reps):
+        run()
+    torch.cuda.synchronize()
+    print(json.dumps({"case": [kind] + dims, "reps": reps, "ok": True}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -467,7 +558,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--case", default=None,
-                    help="M,K,N: run fp8_linear on that one layer a few times and exit")
+                    help="M,K,N: run fp8_linear on that one layer a few times and exit; "
+                         "static,M,K / tensor,M,K / kv,T,H,D: one quantizer variant")
     args = ap.parse_args()
     if args.case:
         return run_case(args.case)

@@ -65,6 +65,15 @@ def lib() -> ctypes.CDLL:
         L.fp8_linear_workspace_size.argtypes = [_i64, _i64, _i64]
         L.fp8_scaled_gemm_workspace_size.restype = ctypes.c_size_t
         L.fp8_scaled_gemm_workspace_size.argtypes = [_i64, _i64, _i64]
+        L.fp8_quant_static.restype = _st
+        L.fp8_quant_static.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _vp, _vp]
+        L.fp8_quant_per_tensor.restype = _st
+        L.fp8_quant_per_tensor.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp,
+                                           ctypes.c_size_t, _vp]
+        L.fp8_quant_per_tensor_workspace_size.restype = ctypes.c_size_t
+        L.fp8_quant_per_tensor_workspace_size.argtypes = [_i64, _i64]
+        L.fp8_kv_cache_quant.restype = _st
+        L.fp8_kv_cache_quant.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _i64, _vp]
         L.fp8_status_string.restype = ctypes.c_char_p
         L.fp8_status_string.argtypes = [_st]
         L.fp8_device_status.restype = _st
@@ -163,6 +172,57 @@ def fp8_linear(x: torch.Tensor, wq: torch.Tensor, s_w: torch.Tensor,
     _check(lib().fp8_linear(_ptr(x), _ptr(wq), _ptr(s_w), _ptr(y), M, N, K,
                             _ptr(workspace), workspace.numel(), _stream(stream)), "fp8_linear")
     return y
+
+
+def fp8_quant_static(x: torch.Tensor, s: torch.Tensor, xq: torch.Tensor | None = None,
+                     s_rows: torch.Tensor | None = None, stream=None):
+    """bf16 [M, K] with a given fp32 scale s [1] -> E4M3 codes uint8 [M, K].
+    If s_rows (fp32 [M]) is given, s is written to every entry."""
+    M, K, ldx = _rows(x, "x")
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    _check(lib().fp8_quant_static(_ptr(x), M, K, ldx, _ptr(s), _ptr(xq),
+                                  xq.stride(0) if M else K, _ptr(s_rows), _stream(stream)),
+           "fp8_quant_static")
+    return xq
+
+
+def fp8_quant_per_tensor(x: torch.Tensor, xq: torch.Tensor | None = None,
+                         s: torch.Tensor | None = None, s_rows: torch.Tensor | None = None,
+                         workspace: torch.Tensor | None = None, stream=None):
+    """bf16 [M, K] -> (E4M3 codes uint8 [M, K], fp32 scale [1]) with one
+    dynamic scale amax / 448 for the whole tensor."""
+    M, K, ldx = _rows(x, "x")
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if s is None:
+        s = torch.empty((1,), dtype=torch.float32, device=x.device)
+    need = int(lib().fp8_quant_per_tensor_workspace_size(M, K))
+    if workspace is None:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=x.device)
+    _check(lib().fp8_quant_per_tensor(_ptr(x), M, K, ldx, _ptr(xq), xq.stride(0) if M else K,
+                                      _ptr(s), _ptr(s_rows), _ptr(workspace), workspace.numel(),
+                                      _stream(stream)), "fp8_quant_per_tensor")
+    return xq, s
+
+
+def fp8_kv_cache_quant(kv: torch.Tensor, scale: torch.Tensor, cache: torch.Tensor,
+                       slot_mapping: torch.Tensor | None = None, stream=None):
+    """Write bf16 keys or values [T, H, D] into the E4M3 cache [n_slots, H, D]
+    (uint8) at rows slot_mapping [T] (int64; negative skips), each head h
+    divided by scale[h] (per-head, [H]) or scale[0] (per-tensor, [1])."""
+    if kv.dim() != 3 or not kv.is_contiguous() or cache.dim() != 3 or not cache.is_contiguous():
+        raise ValueError("kv and cache must be contiguous [T, H, D] / [n_slots, H, D]")
+    T, H, D = kv.shape
+    if cache.shape[1:] != (H, D):
+        raise ValueError("cache must be [n_slots, H, D]")
+    stride = 1 if scale.numel() == H and H > 1 else 0
+    if stride == 0 and scale.numel() != 1:
+        raise ValueError("scale must have 1 or H entries")
+    _check(lib().fp8_kv_cache_quant(_ptr(kv), T, H, D, _ptr(scale), stride, _ptr(slot_mapping),
+                                    _ptr(cache), cache.shape[0], _stream(stream)),
+           "fp8_kv_cache_quant")
+    return cache
 
 
 class QuantizedLinear:

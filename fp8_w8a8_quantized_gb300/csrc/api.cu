@@ -2,7 +2,8 @@
 //
 // This file only validates arguments on the host, keeps a little per-device
 // state (SM count, the device status word, kernel attributes) and launches
-// the kernels of quant.cu, gemm_prefill.cu and gemm_decode.cu.  It never
+// the kernels of quant.cu, quant_variants.cu, gemm_prefill.cu and
+// gemm_decode.cu.  It never
 // allocates device memory and never synchronizes, except in
 // fp8_device_status().
 #include <cuda.h>
@@ -235,6 +236,64 @@ fp8_status_t fp8_linear(const void* x_bf16, const uint8_t* wq, const float* s_w,
     // the GEMM starts: it may stream weights before its own wait, and reads
     // the quantized activations after it.
     return run_gemm(xq, s_tok, wq, s_w, y_bf16, M, N, K, true, stream, d);
+}
+
+fp8_status_t fp8_quant_static(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,
+                              const float* s, uint8_t* xq, int64_t ldq, float* s_rows,
+                              void* stream) {
+    fp8_status_t st = check_quant(x_bf16, M, K, ldx, xq, ldq, s);
+    if (st != FP8_OK || M == 0) return st;
+    if (s_rows && !aligned(s_rows, 4)) return FP8_ERR_UNSUPPORTED;
+    DeviceState* d = nullptr;
+    if ((st = current_device(&d)) != FP8_OK) return st;
+    cudaError_t e = fp8k::launch_quant_given_scale(x_bf16, M, K, ldx, s, xq, ldq, s_rows,
+                                                   d->num_sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+size_t fp8_quant_per_tensor_workspace_size(int64_t M, int64_t K) {
+    (void)M;
+    (void)K;
+    return sizeof(float) * fp8k::kMaxTensorPartials;
+}
+
+fp8_status_t fp8_quant_per_tensor(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,
+                                  uint8_t* xq, int64_t ldq, float* s_out, float* s_rows,
+                                  void* workspace, size_t ws_bytes, void* stream) {
+    fp8_status_t st = check_quant(x_bf16, M, K, ldx, xq, ldq, s_out);
+    if (st != FP8_OK || M == 0) return st;
+    if (s_rows && !aligned(s_rows, 4)) return FP8_ERR_UNSUPPORTED;
+    if (!workspace || ws_bytes < fp8_quant_per_tensor_workspace_size(M, K) ||
+        !aligned(workspace, 16))
+        return FP8_ERR_WORKSPACE;
+    DeviceState* d = nullptr;
+    if ((st = current_device(&d)) != FP8_OK) return st;
+    cudaError_t e = fp8k::launch_quant_per_tensor(x_bf16, M, K, ldx, xq, ldq, s_out, s_rows,
+                                                  static_cast<float*>(workspace), d->num_sms,
+                                                  static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+fp8_status_t fp8_kv_cache_quant(const void* kv_bf16, int64_t T, int64_t H, int64_t D,
+                                const float* scale, int64_t scale_stride,
+                                const int64_t* slot_mapping, uint8_t* cache, int64_t n_slots,
+                                void* stream) {
+    if (T < 0 || H < 0 || D < 0 || n_slots < 0 || scale_stride < 0 || T > kMaxDim ||
+        H > kMaxDim || D > kMaxDim || n_slots > kMaxDim)
+        return FP8_ERR_INVALID_ARG;
+    if (T == 0 || H == 0 || D == 0 || n_slots == 0) return FP8_OK;
+    if (!kv_bf16 || !scale || !cache) return FP8_ERR_INVALID_ARG;
+    if (D % 16 != 0) return FP8_ERR_UNSUPPORTED;
+    if (!aligned(kv_bf16, 16) || !aligned(cache, 16) || !aligned(scale, 4) ||
+        (slot_mapping && !aligned(slot_mapping, 8)))
+        return FP8_ERR_UNSUPPORTED;
+    DeviceState* d = nullptr;
+    fp8_status_t st = current_device(&d);
+    if (st != FP8_OK) return st;
+    cudaError_t e = fp8k::launch_kv_cache_quant(kv_bf16, T, H, D, scale, scale_stride,
+                                                slot_mapping, cache, n_slots, d->num_sms,
+                                                static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
 const char* fp8_status_string(fp8_status_t status) {

@@ -46,6 +46,22 @@ cudaError_t launch_gemm_prefill(const GemmArgs& a);
 constexpr int kDecodeMaxM = 64;
 cudaError_t launch_gemm_decode(const GemmArgs& a);
 
+// Quantization with other scale granularities (quant_variants.cu).
+// Every row quantized with the scale *s; s_rows (optional) gets s per row.
+cudaError_t launch_quant_given_scale(const void* x, int64_t R, int64_t K, int64_t ldx,
+                                     const float* s, uint8_t* q, int64_t ldq, float* s_rows,
+                                     int num_sms, cudaStream_t st);
+// One dynamic scale for the whole tensor; `partial` holds kMaxTensorPartials floats.
+constexpr int kMaxTensorPartials = 2048;
+cudaError_t launch_quant_per_tensor(const void* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q,
+                                    int64_t ldq, float* s_out, float* s_rows, float* partial,
+                                    int num_sms, cudaStream_t st);
+// KV-cache write: x [T, H, D] -> cache[slot[t] (or t), h, :] with scale
+// scale[h * scale_stride]; tokens whose slot is negative or >= n_slots are skipped.
+cudaError_t launch_kv_cache_quant(const void* x, int64_t T, int64_t H, int64_t D,
+                                  const float* scale, int64_t scale_stride, const int64_t* slot,
+                                  uint8_t* cache, int64_t n_slots, int num_sms, cudaStream_t st);
+
 // One-time per-device kernel attribute setup (dynamic shared memory limits).
 cudaError_t prepare_gemm_prefill();
 cudaError_t prepare_gemm_decode();

@@ -1,6 +1,6 @@
-// Per-token E4M3 quantization arithmetic shared by the standalone quantizer
-// (quant.cu) and the fused decode layer (linear_decode.cu), so both produce
-// the same bytes:
+// E4M3 quantization arithmetic shared by the per-token quantizer (quant.cu)
+// and the quantizers with other scale granularities (quant_variants.cu), so
+// all produce the same bytes:
 //   amax = max |x| (exact in fp32), s = amax / 448 (IEEE fp32 division) or 1,
 //   q = E4M3_rn_satfinite(x / s) (IEEE fp32 quotient).
 // "FP8 Inference Explained, in depth", "Scales and their granularity";

@@ -1,0 +1,190 @@
+// Quantization with scales other than one per token:
+//   * a given (static, calibrated) scale: q = E4M3_rn_sat(x / s)
+//     ("Quantization: FP8 inference and KV-cache quantization", "Dynamic
+//     scales or static scales": no run-time reduction; values beyond 448 s
+//     clip to +-448);
+//   * one dynamic scale for the whole tensor, s = amax(all) / 448
+//     ("FP8 Quantization", "Choose Scaling Strategy" and "Granularity");
+//   * FP8 KV-cache writes with a per-tensor or per-head scale, scattered to
+//     cache slots ("Quantization: FP8 inference and KV-cache quantization",
+//     "Turning it on in an engine").
+// The arithmetic is that of the per-token quantizer (quant_math.cuh).  All
+// are grid-stride loops over 16-element chunks (one 32-byte load, one 16-byte
+// store), memory-bound; the per-tensor amax is two launches (per-CTA maxima,
+// then every CTA reduces them), which needs no atomics and no zeroed memory.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "launch.h"
+#include "ptx.cuh"
+#include "quant_math.cuh"
+
+namespace fp8k {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ uint4 quant16(const uint4* src, float s) {
+    const uint4 a = __ldg(src), b = __ldg(src + 1);
+    const uint2 qa = quant8(a, s), qb = quant8(b, s);
+    return make_uint4(qa.x, qa.y, qb.x, qb.y);
+}
+
+// x [R, K] (ld ldx elements) / s -> q [R, K] (ld ldq bytes), grid-stride
+// over 16-element chunks.
+__device__ __forceinline__ void quant_chunks(const uint16_t* __restrict__ x, int64_t R, int64_t K,
+                                             int64_t ldx, float s, uint8_t* __restrict__ q,
+                                             int64_t ldq) {
+    const int64_t C = K >> 4;
+    const int64_t total = R * C;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * kThreads) {
+        const int64_t r = i / C, c = i - r * C;
+        const uint4* src = reinterpret_cast<const uint4*>(x + r * ldx + c * 16);
+        *reinterpret_cast<uint4*>(q + r * ldq + c * 16) = quant16(src, s);
+    }
+}
+
+// s for every row (the per-row scale vector the scaled GEMM consumes).
+__device__ __forceinline__ void fill_rows(float* __restrict__ s_rows, int64_t R, float s) {
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; r < R;
+         r += static_cast<int64_t>(gridDim.x) * kThreads)
+        s_rows[r] = s;
+}
+
+// Static scale: every row divided by *s_ptr.
+__global__ void __launch_bounds__(kThreads)
+    quant_given_scale(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx,
+                      const float* __restrict__ s_ptr, uint8_t* __restrict__ q, int64_t ldq,
+                      float* __restrict__ s_rows) {
+    pdl_wait_primary();
+    pdl_launch_dependents();
+    const float s = __ldg(s_ptr);
+    quant_chunks(x, R, K, ldx, s, q, ldq);
+    if (s_rows) fill_rows(s_rows, R, s);
+}
+
+__device__ __forceinline__ float block_max(float m, float* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane_id() == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    float r = red[0];
+#pragma unroll
+    for (int w = 1; w < kThreads / 32; ++w) r = fmaxf(r, red[w]);
+    __syncthreads();
+    return r;
+}
+
+// Pass 1 of the per-tensor scale: partial[b] = max |x| over this CTA's chunks.
+__global__ void __launch_bounds__(kThreads)
+    tensor_amax_partial(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx,
+                        float* __restrict__ partial) {
+    __shared__ float red[kThreads / 32];
+    pdl_wait_primary();
+    pdl_launch_dependents();
+    const int64_t C = K >> 4;
+    const int64_t total = R * C;
+    float m = 0.0f;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * kThreads) {
+        const int64_t r = i / C, c = i - r * C;
+        const uint4* src = reinterpret_cast<const uint4*>(x + r * ldx + c * 16);
+        m = amax8(__ldg(src + 1), amax8(__ldg(src), m));
+    }
+    m = block_max(m, red);
+    if (threadIdx.x == 0) partial[blockIdx.x] = m;
+}
+
+// Pass 2: every CTA reduces the partial maxima (a fixed, order-independent
+// max), forms s = amax / 448 (1 if zero) and quantizes its chunks.
+__global__ void __launch_bounds__(kThreads)
+    tensor_quant(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx,
+                 const float* __restrict__ partial, int n_partial, uint8_t* __restrict__ q,
+                 int64_t ldq, float* __restrict__ s_out, float* __restrict__ s_rows) {
+    __shared__ float red[kThreads / 32];
+    pdl_wait_primary();
+    pdl_launch_dependents();
+    float m = 0.0f;
+    for (int i = threadIdx.x; i < n_partial; i += kThreads) m = fmaxf(m, partial[i]);
+    const float s = scale_of(block_max(m, red));
+    if (blockIdx.x == 0 && threadIdx.x == 0) *s_out = s;
+    quant_chunks(x, R, K, ldx, s, q, ldq);
+    if (s_rows) fill_rows(s_rows, R, s);
+}
+
+// KV-cache write: x [T, H, D] bf16 -> cache[slot[t], h, :] E4M3 with scale
+// scale[h * scale_stride]; slot < 0 skips the token.
+__global__ void __launch_bounds__(kThreads)
+    kv_cache_quant(const uint16_t* __restrict__ x, int64_t T, int64_t H, int64_t D,
+                   const float* __restrict__ scale, int64_t scale_stride,
+                   const int64_t* __restrict__ slot, uint8_t* __restrict__ cache,
+                   int64_t n_slots) {
+    pdl_wait_primary();
+    pdl_launch_dependents();
+    const int64_t C = D >> 4;  // chunks per head
+    const int64_t total = T * H * C;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * kThreads) {
+        const int64_t th = i / C, c = i - th * C;
+        const int64_t t = th / H, h = th - t * H;
+        const int64_t row = slot ? __ldg(slot + t) : t;
+        if (row < 0 || row >= n_slots) continue;
+        const float s = __ldg(scale + h * scale_stride);
+        const uint4* src = reinterpret_cast<const uint4*>(x + th * D + c * 16);
+        *reinterpret_cast<uint4*>(cache + (row * H + h) * D + c * 16) = quant16(src, s);
+    }
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch(void (*kernel)(Params...), int64_t grid, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = st;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+int64_t grid_for(int64_t chunks, int num_sms) {
+    const int64_t want = (chunks + kThreads - 1) / kThreads;
+    int64_t cap = static_cast<int64_t>(num_sms) * 8;  // 8 x 256 threads per SM
+    if (cap > kMaxTensorPartials) cap = kMaxTensorPartials;
+    return want < 1 ? 1 : (want < cap ? want : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_quant_given_scale(const void* x, int64_t R, int64_t K, int64_t ldx,
+                                     const float* s, uint8_t* q, int64_t ldq, float* s_rows,
+                                     int num_sms, cudaStream_t st) {
+    return launch(quant_given_scale, grid_for(R * (K >> 4), num_sms), st,
+                  static_cast<const uint16_t*>(x), R, K, ldx, s, q, ldq, s_rows);
+}
+
+cudaError_t launch_quant_per_tensor(const void* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q,
+                                    int64_t ldq, float* s_out, float* s_rows, float* partial,
+                                    int num_sms, cudaStream_t st) {
+    const int64_t grid = grid_for(R * (K >> 4), num_sms);
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    cudaError_t e = launch(tensor_amax_partial, grid, st, xb, R, K, ldx, partial);
+    if (e != cudaSuccess) return e;
+    return launch(tensor_quant, grid, st, xb, R, K, ldx, static_cast<const float*>(partial),
+                  static_cast<int>(grid), q, ldq, s_out, s_rows);
+}
+
+cudaError_t launch_kv_cache_quant(const void* x, int64_t T, int64_t H, int64_t D,
+                                  const float* scale, int64_t scale_stride, const int64_t* slot,
+                                  uint8_t* cache, int64_t n_slots, int num_sms, cudaStream_t st) {
+    return launch(kv_cache_quant, grid_for(T * H * (D >> 4), num_sms), st,
+                  static_cast<const uint16_t*>(x), T, H, D, scale, scale_stride, slot, cache,
+                  n_slots);
+}
+
+}  // namespace fp8k

@@ -174,6 +174,68 @@ FP8_API fp8_status_t fp8_linear_static_scratch(const void* x_bf16, const uint8_t
                                                const float* s_w, void* y_bf16, int64_t M,
                                                int64_t N, int64_t K, void* stream);
 
+/*
+ * Quantization with a given (static, calibrated) per-tensor scale:
+ *   q[m,k] = E4M3_rn_satfinite(x[m,k] / s)   (IEEE fp32 quotient)
+ * Source: "Quantization: FP8 inference and KV-cache quantization", "Dynamic
+ * scales or static scales" (a scale fixed from calibration costs nothing at
+ * run time; values beyond 448 s clip to +-448 in saturating mode).
+ *
+ *   x_bf16, M, K, ldx, xq, ldq   as for fp8_quant_per_token
+ *   s       [device, in]  fp32 [1], the scale
+ *   s_rows  [device, out] fp32 [M] or NULL: s written for every row, so the
+ *                         codes can go straight to fp8_scaled_gemm
+ * Requirements as for fp8_quant_per_token; s 4-byte aligned, s > 0 finite.
+ */
+FP8_API fp8_status_t fp8_quant_static(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,
+                                      const float* s, uint8_t* xq, int64_t ldq, float* s_rows,
+                                      void* stream);
+
+/*
+ * Dynamic per-tensor quantization: one scale for the whole [M, K] tensor,
+ *   s = amax_{m,k} |x| / 448 (IEEE fp32 division; 1 if the tensor is zero),
+ *   q[m,k] = E4M3_rn_satfinite(x[m,k] / s).
+ * Source: "FP8 Quantization", "Choose Scaling Strategy" (dynamic scaling from
+ * max |X| on the fly) and "Granularity" (per-tensor: one scale for the entire
+ * matrix).  Two launches; bit-identical results on every call.
+ *
+ *   x_bf16, M, K, ldx, xq, ldq   as for fp8_quant_per_token
+ *   s_out   [device, out] fp32 [1]
+ *   s_rows  [device, out] fp32 [M] or NULL (s for every row, as above)
+ *   workspace [device]    fp8_quant_per_tensor_workspace_size() bytes,
+ *                         16-byte aligned (per-CTA maxima)
+ */
+FP8_API fp8_status_t fp8_quant_per_tensor(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,
+                                          uint8_t* xq, int64_t ldq, float* s_out, float* s_rows,
+                                          void* workspace, size_t ws_bytes, void* stream);
+
+/* Workspace bytes of fp8_quant_per_tensor (a fixed 8 KB). */
+FP8_API size_t fp8_quant_per_tensor_workspace_size(int64_t M, int64_t K);
+
+/*
+ * FP8 KV-cache write (quantize on write): for every token t, head h, and
+ * d < D,
+ *   cache[slot[t], h, d] = E4M3_rn_satfinite(kv[t, h, d] / scale[h * scale_stride])
+ * Source: "Quantization: FP8 inference and KV-cache quantization", "Turning
+ * it on in an engine" (one scale per tensor or per attention head, 1.0 when
+ * uncalibrated; values beyond 448 are clipped) and "FP8 Inference Explained,
+ * in depth", "FP8 KV cache".
+ *
+ *   kv_bf16 [device, in]  bf16 [T, H, D], contiguous (keys or values)
+ *   scale   [device, in]  fp32: [H] with scale_stride 1 (per head) or [1]
+ *                         with scale_stride 0 (per tensor)
+ *   slot_mapping [device, in] int64 [T] or NULL (token t -> row t); a token
+ *                         whose slot is negative or >= n_slots is skipped;
+ *                         slots must be distinct (two tokens writing one
+ *                         slot leave an unspecified mix of their codes)
+ *   cache   [device, out] E4M3 [n_slots, H, D], contiguous
+ * Requirements: D % 16 == 0; kv_bf16 and cache 16-byte aligned.
+ */
+FP8_API fp8_status_t fp8_kv_cache_quant(const void* kv_bf16, int64_t T, int64_t H, int64_t D,
+                                        const float* scale, int64_t scale_stride,
+                                        const int64_t* slot_mapping, uint8_t* cache,
+                                        int64_t n_slots, void* stream);
+
 /* Workspace bytes fp8_linear needs for an [M, K] x [N, K]^T layer:
  * round_up(M*K, 256) + round_up(4*M, 256).  0 for invalid sizes. */
 FP8_API size_t fp8_linear_workspace_size(int64_t M, int64_t N, int64_t K);

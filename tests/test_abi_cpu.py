@@ -94,3 +94,33 @@ def test_product_path_does_not_import_the_oracle():
             text = open(path).read()
             assert "import oracle" not in text and "from oracle" not in text, path
             assert "fp8_oracle" not in text and "orc_" not in text, path
+
+
+def test_host_checks_of_the_scale_variants(L):
+    INVALID, UNSUP, WS = 1, 2, 3
+    fake = 1 << 20
+    # static scale: x, M, K, ldx, s, xq, ldq, s_rows, stream
+    assert L.fp8_quant_static(fake, 4, 32, 32, None, fake, 32, None, None) == INVALID
+    assert L.fp8_quant_static(fake, 4, 24, 24, fake, fake, 32, None, None) == UNSUP
+    assert L.fp8_quant_static(fake, 4, 32, 32, fake, fake, 32, fake + 2, None) == UNSUP
+    assert L.fp8_quant_static(fake, 4, 32, 32, fake + 1, fake, 32, None, None) == UNSUP
+    assert L.fp8_quant_static(fake, 0, 32, 32, fake, fake, 32, None, None) == 0
+    # dynamic per-tensor: ..., s_out, s_rows, workspace, ws_bytes, stream
+    assert L.fp8_quant_per_tensor_workspace_size(4096, 4096) == 8192
+    assert L.fp8_quant_per_tensor(fake, 4, 32, 32, fake, 32, None, None, fake, 8192, None) == INVALID
+    assert L.fp8_quant_per_tensor(fake, 4, 32, 32, fake, 32, fake, None, None, 0, None) == WS
+    assert L.fp8_quant_per_tensor(fake, 4, 32, 32, fake, 32, fake, None, fake, 100, None) == WS
+    assert L.fp8_quant_per_tensor(fake, 4, 32, 32, fake, 32, fake, None, fake + 4, 8192, None) == WS
+    assert L.fp8_quant_per_tensor(fake, 4, 40, 40, fake, 48, fake, None, fake, 8192, None) == UNSUP
+    assert L.fp8_quant_per_tensor(fake, 0, 32, 32, fake, 32, fake, None, None, 0, None) == 0
+    # KV cache: kv, T, H, D, scale, scale_stride, slot, cache, n_slots, stream
+    assert L.fp8_kv_cache_quant(fake, 4, 8, 24, fake, 1, None, fake, 16, None) == UNSUP
+    assert L.fp8_kv_cache_quant(None, 4, 8, 128, fake, 1, None, fake, 16, None) == INVALID
+    assert L.fp8_kv_cache_quant(fake, 4, 8, 128, None, 1, None, fake, 16, None) == INVALID
+    assert L.fp8_kv_cache_quant(fake, -1, 8, 128, fake, 1, None, fake, 16, None) == INVALID
+    assert L.fp8_kv_cache_quant(fake, 4, 8, 128, fake, -1, None, fake, 16, None) == INVALID
+    assert L.fp8_kv_cache_quant(fake, 4, 8, 128, fake, 1, fake + 4, fake, 16, None) == UNSUP
+    assert L.fp8_kv_cache_quant(fake, 4, 8, 128, fake, 1, None, fake + 8, 16, None) == UNSUP
+    assert L.fp8_kv_cache_quant(fake, 4, 8, 128, fake + 2, 1, None, fake, 16, None) == UNSUP
+    assert L.fp8_kv_cache_quant(fake, 0, 8, 128, fake, 1, None, fake, 16, None) == 0
+    assert L.fp8_kv_cache_quant(fake, 4, 8, 128, fake, 1, None, fake, 0, None) == 0
