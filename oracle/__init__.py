@@ -93,6 +93,11 @@ def _load():
         lib.orc_quant_tensor_bf16.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp]
         lib.orc_kv_cache_quant_bf16.restype = None
         lib.orc_kv_cache_quant_bf16.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp]
+        lib.orc_quant_blocks_bf16.restype = None
+        lib.orc_quant_blocks_bf16.argtypes = [_vp, _i64, _i64, _i64, _i64, _i64, _vp, _i64, _vp]
+        lib.orc_gemm_blockwise.restype = None
+        lib.orc_gemm_blockwise.argtypes = [_vp, _i64, _vp, _vp, _i64, _vp, _i64, _i64, _i64,
+                                           _i64, _i64, _i64, _vp, _vp, _vp]
         lib.orc_num_threads.restype = ctypes.c_int
         lib.orc_num_threads.argtypes = []
         _lib = lib
@@ -281,4 +286,65 @@ def linear_points(qx, s_tok, qw, s_w, rows, cols) -> np.ndarray:
     if r.size:
         lib.orc_linear_points(_ptr(a), K, _ptr(st), _ptr(b), K, _ptr(sw), K,
                               r.size, _ptr(r), _ptr(c), _ptr(y))
+    return y
+
+
+# --------------------------------------------------------------------------
+# Block-wise scales
+# --------------------------------------------------------------------------
+
+GROUP = 128   # activation group length along K and weight block edge
+
+
+def quant_blocks_bf16(x_bits: np.ndarray, br: int, bk: int):
+    """Block-wise quantization of bf16 bits [R, K]: one scale per br x bk
+    block (partial at the edges).  Returns (codes [R, K], scales
+    [ceil(R/br), ceil(K/bk)])."""
+    lib = _load()
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    R, K = x.shape
+    RB, KB = -(-R // br), -(-K // bk)
+    q = np.empty((R, K), dtype=np.uint8)
+    s = np.empty((RB, KB), dtype=np.float32)
+    if R and K:
+        lib.orc_quant_blocks_bf16(_ptr(x), R, K, K, br, bk, _ptr(q), K, _ptr(s))
+    return q, s
+
+
+def quant_groups_bf16(x_bits: np.ndarray, group: int = GROUP):
+    """Activations: one scale per token per `group` inputs, s [M, ceil(K/group)]."""
+    return quant_blocks_bf16(x_bits, 1, group)
+
+
+def quant_weight_blocks_bf16(w_bits: np.ndarray, block: int = GROUP):
+    """Weights: one scale per block x block tile, s [ceil(N/block), ceil(K/block)]."""
+    return quant_blocks_bf16(w_bits, block, block)
+
+
+def gemm_blockwise(qx, s_x, qw, s_w, bn: int = GROUP, bk: int = GROUP,
+                   rows=None, cols=None) -> np.ndarray:
+    """y = sum_kb s_x[m,kb] s_w[n//bn,kb] (exact block dot product), fp64.
+    Full [M, N] output, or the values at the (rows[i], cols[i]) points."""
+    lib = _load()
+    a = np.ascontiguousarray(qx, dtype=np.uint8)
+    b = np.ascontiguousarray(qw, dtype=np.uint8)
+    sx = np.ascontiguousarray(s_x, dtype=np.float32)
+    sw = np.ascontiguousarray(s_w, dtype=np.float32)
+    M, K = a.shape
+    N, K2 = b.shape
+    assert K == K2
+    KB = -(-K // bk)
+    assert sx.shape == (M, KB) and sw.shape == (-(-N // bn), KB)
+    if rows is None:
+        y = np.zeros((M, N), dtype=np.float64)
+        if M and N:
+            lib.orc_gemm_blockwise(_ptr(a), K, _ptr(sx), _ptr(b), K, _ptr(sw), M, N, K, bn, bk,
+                                   0, None, None, _ptr(y))
+        return y
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    c = np.ascontiguousarray(cols, dtype=np.int64)
+    y = np.zeros(r.shape, dtype=np.float64)
+    if r.size:
+        lib.orc_gemm_blockwise(_ptr(a), K, _ptr(sx), _ptr(b), K, _ptr(sw), M, N, K, bn, bk,
+                               r.size, _ptr(r), _ptr(c), _ptr(y))
     return y

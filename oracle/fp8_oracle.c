@@ -354,3 +354,90 @@ void orc_kv_cache_quant_bf16(const uint16_t* x, int64_t T, int64_t H, int64_t D,
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Block-wise scales: 1 x G activation groups, Bn x Bk weight blocks         */
+/* ------------------------------------------------------------------------ */
+
+/* Each rectangle [r0, r1) x [k0, k1) of x shares one scale:
+ * s = fl32(amax / 448) (1 if the rectangle is all zero) and every value in it
+ * becomes E4M3(fl32(x / s)) -- the per-token rule applied to a smaller set of
+ * values ("FP8 Quantization", "Granularity": per-block, one scale per
+ * 128 x 128 tile; "FP8 Inference Explained, in depth", "Scales and their
+ * granularity": s = amax / 448 where amax is the largest value the scale
+ * covers). */
+static float quant_rect_bf16(const uint16_t* x, int64_t ldx, int64_t r0, int64_t r1,
+                             int64_t k0, int64_t k1, uint8_t* q, int64_t ldq)
+{
+    float amax = 0.0f, s;
+    int64_t r, k;
+    for (r = r0; r < r1; ++r)
+        for (k = k0; k < k1; ++k) {
+            float a = fabsf(bf16_to_f32(x[r * ldx + k]));
+            if (a > amax)
+                amax = a;
+        }
+    s = (amax > 0.0f) ? amax / 448.0f : 1.0f;
+    for (r = r0; r < r1; ++r)
+        for (k = k0; k < k1; ++k) {
+            volatile float t = bf16_to_f32(x[r * ldx + k]) / s;
+            q[r * ldq + k] = orc_e4m3_encode((double)t);
+        }
+    return s;
+}
+
+/* x [R, K] in blocks of br rows x bk columns (the last block of each
+ * dimension may be partial).  s is [ceil(R/br), ceil(K/bk)] row-major.
+ * Activations use br = 1, bk = 128 (one scale per token per 128 inputs);
+ * weights use br = bk = 128. */
+void orc_quant_blocks_bf16(const uint16_t* x, int64_t R, int64_t K, int64_t ldx,
+                           int64_t br, int64_t bk, uint8_t* q, int64_t ldq, float* s)
+{
+    const int64_t RB = (R + br - 1) / br, KB = (K + bk - 1) / bk;
+    int64_t b;
+#pragma omp parallel for schedule(dynamic, 8)
+    for (b = 0; b < RB * KB; ++b) {
+        const int64_t rb = b / KB, kb = b % KB;
+        const int64_t r0 = rb * br, k0 = kb * bk;
+        const int64_t r1 = r0 + br < R ? r0 + br : R, k1 = k0 + bk < K ? k0 + bk : K;
+        s[b] = quant_rect_bf16(x, ldx, r0, r1, k0, k1, q, ldq);
+    }
+}
+
+/* Block-scaled GEMM ("FP8 Inference Explained, in depth", "Inside a quantized
+ * linear layer": block-wise scales vary along k, so each block's partial sum
+ * is multiplied by that block's scales before the partial sums are added):
+ *   y[m,n] = sum_kb  s_x[m, kb] * s_w[n / bn, kb] * P[m, n, kb],
+ *   P[m, n, kb] = sum_{k in block kb} e4m3(q_x[m,k]) * e4m3(q_w[n,k]),
+ * blocks of bk along K for both operands.  Each P is exact (int64 of codes
+ * times 2^9), the sum over kb is in fp64, in increasing kb.  Computed at the
+ * npts points (rows[p], cols[p]) only, or everywhere when rows is NULL
+ * (then y is [M, N]). */
+void orc_gemm_blockwise(const uint8_t* qx, int64_t ldqx, const float* s_x,
+                        const uint8_t* qw, int64_t ldqw, const float* s_w,
+                        int64_t M, int64_t N, int64_t K, int64_t bn, int64_t bk,
+                        int64_t npts, const int64_t* rows, const int64_t* cols, double* y)
+{
+    const int64_t KB = (K + bk - 1) / bk;
+    const int64_t total = rows ? npts : M * N;
+    int64_t tab[256];
+    int64_t p;
+    int i;
+    for (i = 0; i < 256; ++i)
+        tab[i] = ((i & 0x7F) == 0x7F) ? 0 : code_times_512((uint8_t)i);
+#pragma omp parallel for schedule(static)
+    for (p = 0; p < total; ++p) {
+        const int64_t m = rows ? rows[p] : p / N, n = rows ? cols[p] : p % N;
+        double acc = 0.0;
+        int64_t kb, k;
+        for (kb = 0; kb < KB; ++kb) {
+            const int64_t k1 = (kb + 1) * bk < K ? (kb + 1) * bk : K;
+            int64_t part = 0;
+            for (k = kb * bk; k < k1; ++k)
+                part += tab[qx[m * ldqx + k]] * tab[qw[n * ldqw + k]];
+            acc += ldexp((double)part, -18) * (double)s_x[m * KB + kb]
+                   * (double)s_w[(n / bn) * KB + kb];
+        }
+        y[p] = acc;
+    }
+}
