@@ -74,6 +74,18 @@ def lib() -> ctypes.CDLL:
         L.fp8_quant_per_tensor_workspace_size.argtypes = [_i64, _i64]
         L.fp8_kv_cache_quant.restype = _st
         L.fp8_kv_cache_quant.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _i64, _vp]
+        L.fp8_quant_per_token_group.restype = _st
+        L.fp8_quant_per_token_group.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp]
+        L.fp8_quant_weight_blocks.restype = _st
+        L.fp8_quant_weight_blocks.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp]
+        L.fp8_scaled_gemm_blockwise.restype = _st
+        L.fp8_scaled_gemm_blockwise.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp,
+                                                ctypes.c_size_t, _vp]
+        L.fp8_linear_blockwise.restype = _st
+        L.fp8_linear_blockwise.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp,
+                                           ctypes.c_size_t, _vp]
+        L.fp8_linear_blockwise_workspace_size.restype = ctypes.c_size_t
+        L.fp8_linear_blockwise_workspace_size.argtypes = [_i64, _i64, _i64]
         L.fp8_status_string.restype = ctypes.c_char_p
         L.fp8_status_string.argtypes = [_st]
         L.fp8_device_status.restype = _st
@@ -223,6 +235,76 @@ def fp8_kv_cache_quant(kv: torch.Tensor, scale: torch.Tensor, cache: torch.Tenso
                                     _ptr(cache), cache.shape[0], _stream(stream)),
            "fp8_kv_cache_quant")
     return cache
+
+
+BLOCK = 128  # edge of the block-wise scales
+
+
+def _blocks(n: int) -> int:
+    return (n + BLOCK - 1) // BLOCK
+
+
+def fp8_quant_per_token_group(x: torch.Tensor, xq: torch.Tensor | None = None,
+                              s_x: torch.Tensor | None = None, stream=None):
+    """bf16 [M, K] -> (codes uint8 [M, K], fp32 scales [M, ceil(K/128)]),
+    one scale per token per 128 inputs."""
+    M, K, ldx = _rows(x, "x")
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if s_x is None:
+        s_x = torch.empty((M, _blocks(K)), dtype=torch.float32, device=x.device)
+    _check(lib().fp8_quant_per_token_group(_ptr(x), M, K, ldx, _ptr(xq), xq.stride(0) if M else K,
+                                           _ptr(s_x), _stream(stream)),
+           "fp8_quant_per_token_group")
+    return xq, s_x
+
+
+def fp8_quant_weight_blocks(w: torch.Tensor, wq: torch.Tensor | None = None,
+                            s_w: torch.Tensor | None = None, stream=None):
+    """bf16 [N, K] -> (codes uint8 [N, K], fp32 scales [ceil(N/128), ceil(K/128)]),
+    one scale per 128 x 128 block."""
+    N, K, ldw = _rows(w, "w")
+    if wq is None:
+        wq = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    if s_w is None:
+        s_w = torch.empty((_blocks(N), _blocks(K)), dtype=torch.float32, device=w.device)
+    _check(lib().fp8_quant_weight_blocks(_ptr(w), N, K, ldw, _ptr(wq), wq.stride(0) if N else K,
+                                         _ptr(s_w), _stream(stream)), "fp8_quant_weight_blocks")
+    return wq, s_w
+
+
+def fp8_scaled_gemm_blockwise(xq: torch.Tensor, s_x: torch.Tensor, wq: torch.Tensor,
+                              s_w: torch.Tensor, y: torch.Tensor | None = None, stream=None):
+    """Block-scaled GEMM: (codes [M, K], s_x [M, KB]) x (codes [N, K], s_w [NB, KB]) -> bf16."""
+    M, K = xq.shape
+    N = wq.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    _check(lib().fp8_scaled_gemm_blockwise(_ptr(xq), _ptr(s_x), _ptr(wq), _ptr(s_w), _ptr(y),
+                                           M, N, K, None, 0, _stream(stream)),
+           "fp8_scaled_gemm_blockwise")
+    return y
+
+
+def fp8_linear_blockwise_workspace_size(M: int, N: int, K: int) -> int:
+    return int(lib().fp8_linear_blockwise_workspace_size(M, N, K))
+
+
+def fp8_linear_blockwise(x: torch.Tensor, wq: torch.Tensor, s_w: torch.Tensor,
+                         y: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                         stream=None):
+    """The block-scaled layer: bf16 X [M, K] and block-quantized W -> bf16 [M, N]."""
+    M, K = x.shape
+    N = wq.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    need = fp8_linear_blockwise_workspace_size(M, N, K)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=x.device)
+    _check(lib().fp8_linear_blockwise(_ptr(x), _ptr(wq), _ptr(s_w), _ptr(y), M, N, K,
+                                      _ptr(workspace), workspace.numel(), _stream(stream)),
+           "fp8_linear_blockwise")
+    return y
 
 
 class QuantizedLinear:

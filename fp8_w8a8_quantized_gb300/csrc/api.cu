@@ -2,8 +2,8 @@
 //
 // This file only validates arguments on the host, keeps a little per-device
 // state (SM count, the device status word, kernel attributes) and launches
-// the kernels of quant.cu, quant_variants.cu, gemm_prefill.cu and
-// gemm_decode.cu.  It never
+// the kernels of quant.cu, quant_variants.cu, gemm_prefill.cu,
+// gemm_decode.cu and gemm_blockwise.cu.  It never
 // allocates device memory and never synchronizes, except in
 // fp8_device_status().
 #include <cuda.h>
@@ -52,7 +52,8 @@ fp8_status_t current_device(DeviceState** out) {
         } else if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word) !=
                        cudaSuccess ||
                    fp8k::prepare_gemm_prefill() != cudaSuccess ||
-                   fp8k::prepare_gemm_decode() != cudaSuccess) {
+                   fp8k::prepare_gemm_decode() != cudaSuccess ||
+                   fp8k::prepare_gemm_blockwise() != cudaSuccess) {
             d.verdict = FP8_ERR_CUDA;
         } else {
             d.verdict = FP8_OK;
@@ -128,7 +129,7 @@ fp8_status_t check_gemm(const uint8_t* xq, const float* s_tok, const uint8_t* wq
 
 fp8_status_t run_gemm(const uint8_t* xq, const float* s_tok, const uint8_t* wq, const float* s_w,
                       void* y, int64_t M, int64_t N, int64_t K, bool after_quant, void* stream,
-                      DeviceState* d) {
+                      DeviceState* d, bool blockwise = false) {
     fp8k::GemmArgs a;
     a.xq = xq;
     a.s_tok = s_tok;
@@ -143,10 +144,15 @@ fp8_status_t run_gemm(const uint8_t* xq, const float* s_tok, const uint8_t* wq, 
     a.pdl = true;
     a.w_early = after_quant;
     a.stream = static_cast<cudaStream_t>(stream);
-    cudaError_t e = M <= fp8k::kDecodeMaxM ? fp8k::launch_gemm_decode(a)
-                                           : fp8k::launch_gemm_prefill(a);
+    cudaError_t e = blockwise                 ? fp8k::launch_gemm_blockwise(a)
+                    : M <= fp8k::kDecodeMaxM ? fp8k::launch_gemm_decode(a)
+                                             : fp8k::launch_gemm_prefill(a);
     return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
+
+constexpr int64_t kScaleBlock = 128;
+
+int64_t blocks_of(int64_t n) { return (n + kScaleBlock - 1) / kScaleBlock; }
 
 }  // namespace
 
@@ -294,6 +300,74 @@ fp8_status_t fp8_kv_cache_quant(const void* kv_bf16, int64_t T, int64_t H, int64
                                                 slot_mapping, cache, n_slots, d->num_sms,
                                                 static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+fp8_status_t fp8_quant_per_token_group(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,
+                                       uint8_t* xq, int64_t ldq, float* s_x, void* stream) {
+    fp8_status_t st = check_quant(x_bf16, M, K, ldx, xq, ldq, s_x);
+    if (st != FP8_OK || M == 0 || K == 0) return st;
+    DeviceState* d = nullptr;
+    if ((st = current_device(&d)) != FP8_OK) return st;
+    cudaError_t e = fp8k::launch_quant_groups(x_bf16, M, K, ldx, xq, ldq, s_x, d->num_sms,
+                                              static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+fp8_status_t fp8_quant_weight_blocks(const void* w_bf16, int64_t N, int64_t K, int64_t ldw,
+                                     uint8_t* wq, int64_t ldwq, float* s_w, void* stream) {
+    fp8_status_t st = check_quant(w_bf16, N, K, ldw, wq, ldwq, s_w);
+    if (st != FP8_OK || N == 0 || K == 0) return st;
+    if (blocks_of(N) > 65535) return FP8_ERR_UNSUPPORTED;
+    DeviceState* d = nullptr;
+    if ((st = current_device(&d)) != FP8_OK) return st;
+    cudaError_t e = fp8k::launch_quant_weight_blocks(w_bf16, N, K, ldw, wq, ldwq, s_w,
+                                                     static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+fp8_status_t fp8_scaled_gemm_blockwise(const uint8_t* xq, const float* s_x, const uint8_t* wq,
+                                       const float* s_w, void* y_bf16, int64_t M, int64_t N,
+                                       int64_t K, void* workspace, size_t ws_bytes,
+                                       void* stream) {
+    (void)workspace;
+    (void)ws_bytes;
+    fp8_status_t st = check_gemm(xq, s_x, wq, s_w, y_bf16, M, N, K);
+    if (st != FP8_OK || M == 0 || N == 0) return st;
+    DeviceState* d = nullptr;
+    if ((st = current_device(&d)) != FP8_OK) return st;
+    return run_gemm(xq, s_x, wq, s_w, y_bf16, M, N, K, false, stream, d, true);
+}
+
+size_t fp8_linear_blockwise_workspace_size(int64_t M, int64_t N, int64_t K) {
+    (void)N;
+    if (M < 0 || K < 0 || M > kMaxDim || K > kMaxDim) return 0;
+    return round_up(static_cast<size_t>(M) * static_cast<size_t>(K), 256) +
+           round_up(4 * static_cast<size_t>(M) * static_cast<size_t>(blocks_of(K)), 256);
+}
+
+fp8_status_t fp8_linear_blockwise(const void* x_bf16, const uint8_t* wq, const float* s_w,
+                                  void* y_bf16, int64_t M, int64_t N, int64_t K, void* workspace,
+                                  size_t ws_bytes, void* stream) {
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return FP8_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return FP8_OK;
+    if (!x_bf16 || !wq || !s_w || !y_bf16) return FP8_ERR_INVALID_ARG;
+    if (K <= 0 || K % 16 != 0) return FP8_ERR_UNSUPPORTED;
+    if (!aligned(x_bf16, 16)) return FP8_ERR_UNSUPPORTED;
+    const size_t need = fp8_linear_blockwise_workspace_size(M, N, K);
+    if (!workspace || ws_bytes < need || !aligned(workspace, 256)) return FP8_ERR_WORKSPACE;
+    uint8_t* xq = static_cast<uint8_t*>(workspace);
+    float* s_x = reinterpret_cast<float*>(xq + round_up(static_cast<size_t>(M) * K, 256));
+    fp8_status_t st = check_gemm(xq, s_x, wq, s_w, y_bf16, M, N, K);
+    if (st != FP8_OK) return st;
+    DeviceState* d = nullptr;
+    if ((st = current_device(&d)) != FP8_OK) return st;
+    cudaError_t e = fp8k::launch_quant_groups(x_bf16, M, K, K, xq, K, s_x, d->num_sms,
+                                              static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return FP8_ERR_CUDA;
+    // as in fp8_linear: the quantizer releases the GEMM only after its own
+    // wait, so the GEMM may stream weights before its griddepcontrol.wait
+    return run_gemm(xq, s_x, wq, s_w, y_bf16, M, N, K, true, stream, d, true);
 }
 
 const char* fp8_status_string(fp8_status_t status) {

@@ -1,6 +1,6 @@
-// Shape constants and helpers shared by the two decode-sized kernels: the
-// scaled GEMM on pre-quantized activations (gemm_decode.cu) and the fused
-// quantize + GEMM layer (linear_decode.cu).
+// Shape constants and helpers shared by the decode-sized (weight-streaming)
+// GEMMs: per-token x per-channel scales (gemm_decode.cu) and block-wise
+// scales (gemm_blockwise.cu).
 #pragma once
 
 #include <cstdint>

@@ -62,8 +62,21 @@ cudaError_t launch_kv_cache_quant(const void* x, int64_t T, int64_t H, int64_t D
                                   const float* scale, int64_t scale_stride, const int64_t* slot,
                                   uint8_t* cache, int64_t n_slots, int num_sms, cudaStream_t st);
 
+// Block-wise scales (quant_variants.cu): activations one scale per token per
+// 128 inputs, s [R, ceil(K/128)]; weights one scale per 128 x 128 block,
+// s [ceil(N/128), ceil(K/128)].
+cudaError_t launch_quant_groups(const void* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q,
+                                int64_t ldq, float* s, int num_sms, cudaStream_t st);
+cudaError_t launch_quant_weight_blocks(const void* w, int64_t N, int64_t K, int64_t ldw,
+                                       uint8_t* q, int64_t ldq, float* s, cudaStream_t st);
+
+// Block-scaled GEMM (gemm_blockwise.cu): GemmArgs with s_tok = s_x
+// [M, ceil(K/128)] and s_w [ceil(N/128), ceil(K/128)].
+cudaError_t launch_gemm_blockwise(const GemmArgs& a);
+
 // One-time per-device kernel attribute setup (dynamic shared memory limits).
 cudaError_t prepare_gemm_prefill();
 cudaError_t prepare_gemm_decode();
+cudaError_t prepare_gemm_blockwise();
 
 }  // namespace fp8k

@@ -25,6 +25,7 @@ namespace fp8k {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int64_t kGroup = 128;  // block edge of the block-wise scales
 
 __device__ __forceinline__ uint4 quant16(const uint4* src, float s) {
     const uint4 a = __ldg(src), b = __ldg(src + 1);
@@ -138,6 +139,79 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// Block-wise activation scales: one scale per token per 128 inputs.  Eight
+// consecutive lanes own a group (one 16-element chunk each), so a warp covers
+// four groups; the loop runs per warp (uniform trip count) and the group
+// maximum is a three-step butterfly within the eight lanes.
+__global__ void __launch_bounds__(kThreads)
+    quant_groups(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx,
+                 uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s, int64_t KB) {
+    pdl_wait_primary();
+    pdl_launch_dependents();
+    const int lane = lane_id();
+    const int sub = lane & 7;
+    const int64_t groups = R * KB;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
+    for (int64_t base = (static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5)) * 4;
+         base < groups; base += warps * 4) {
+        const int64_t g = base + (lane >> 3);
+        const int64_t r = g < groups ? g / KB : 0, kb = g - r * KB;
+        const int64_t k = kb * kGroup + sub * 16;
+        const bool live = g < groups && k < K;
+        uint4 a = make_uint4(0, 0, 0, 0), b = a;
+        const uint4* src = reinterpret_cast<const uint4*>(x + r * ldx + k);
+        if (live) {
+            a = __ldg(src);
+            b = __ldg(src + 1);
+        }
+        float m = amax8(b, amax8(a, 0.0f));
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        const float sc = scale_of(m);
+        if (live) {
+            const uint2 qa = quant8(a, sc), qb = quant8(b, sc);
+            *reinterpret_cast<uint4*>(q + r * ldq + k) = make_uint4(qa.x, qa.y, qb.x, qb.y);
+            if (sub == 0) s[r * KB + kb] = sc;
+        }
+    }
+}
+
+// Block-wise weight scales: one CTA per 128 x 128 block (partial at the
+// edges); each thread holds four 16-element chunks (rows t/8 + 32 i, chunk
+// t % 8) in registers between the block maximum and the quantization.
+__global__ void __launch_bounds__(kThreads)
+    quant_weight_blocks(const uint16_t* __restrict__ w, int64_t N, int64_t K, int64_t ldw,
+                        uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s) {
+    __shared__ float red[kThreads / 32];
+    pdl_wait_primary();
+    pdl_launch_dependents();
+    const int64_t kb = blockIdx.x, nb = blockIdx.y, KB = gridDim.x;
+    const int64_t k = kb * kGroup + (threadIdx.x & 7) * 16;
+    uint4 v[4][2];
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t n = nb * kGroup + (threadIdx.x >> 3) + 32 * i;
+        v[i][0] = v[i][1] = make_uint4(0, 0, 0, 0);
+        if (n < N && k < K) {
+            const uint4* src = reinterpret_cast<const uint4*>(w + n * ldw + k);
+            v[i][0] = __ldg(src);
+            v[i][1] = __ldg(src + 1);
+        }
+        m = amax8(v[i][1], amax8(v[i][0], m));
+    }
+    const float sc = scale_of(block_max(m, red));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t n = nb * kGroup + (threadIdx.x >> 3) + 32 * i;
+        if (n < N && k < K) {
+            const uint2 qa = quant8(v[i][0], sc), qb = quant8(v[i][1], sc);
+            *reinterpret_cast<uint4*>(q + n * ldq + k) = make_uint4(qa.x, qa.y, qb.x, qb.y);
+        }
+    }
+    if (threadIdx.x == 0) s[nb * KB + kb] = sc;
+}
+
 template <typename... Params, typename... Args>
 cudaError_t launch(void (*kernel)(Params...), int64_t grid, cudaStream_t st, Args... args) {
     cudaLaunchConfig_t cfg = {};
@@ -185,6 +259,30 @@ cudaError_t launch_kv_cache_quant(const void* x, int64_t T, int64_t H, int64_t D
     return launch(kv_cache_quant, grid_for(T * H * (D >> 4), num_sms), st,
                   static_cast<const uint16_t*>(x), T, H, D, scale, scale_stride, slot, cache,
                   n_slots);
+}
+
+cudaError_t launch_quant_groups(const void* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q,
+                                int64_t ldq, float* s, int num_sms, cudaStream_t st) {
+    const int64_t KB = (K + kGroup - 1) / kGroup;
+    const int64_t grid = grid_for(R * KB * 8, num_sms);  // eight threads per group
+    return launch(quant_groups, grid, st, static_cast<const uint16_t*>(x), R, K, ldx, q, ldq, s,
+                  KB);
+}
+
+cudaError_t launch_quant_weight_blocks(const void* w, int64_t N, int64_t K, int64_t ldw,
+                                       uint8_t* q, int64_t ldq, float* s, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(static_cast<unsigned>((K + kGroup - 1) / kGroup),
+                       static_cast<unsigned>((N + kGroup - 1) / kGroup));
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = st;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, quant_weight_blocks, static_cast<const uint16_t*>(w), N, K,
+                              ldw, q, ldq, s);
 }
 
 }  // namespace fp8k

@@ -236,6 +236,62 @@ FP8_API fp8_status_t fp8_kv_cache_quant(const void* kv_bf16, int64_t T, int64_t 
                                         const int64_t* slot_mapping, uint8_t* cache,
                                         int64_t n_slots, void* stream);
 
+/*
+ * Block-wise scales.  Source: "FP8 Quantization", "Granularity" (per-block:
+ * one scale per 128 x 128 weight tile) and "FP8 Inference Explained, in
+ * depth", "Inside a quantized linear layer" (block-wise scales vary along k,
+ * so each block's partial sum is multiplied by its scales before the partial
+ * sums are added).  Reading: activations take one scale per token per 128
+ * inputs (the 128-element promotion interval of "Quantization: FP8 inference
+ * and KV-cache quantization", "Training in FP8 or lower"); every block uses
+ * the per-token rule, s = fl32(amax / 448) (1 if the block is all zero) and
+ * q = E4M3_rn_satfinite(fl32(x / s)).  KB = ceil(K / 128), NB = ceil(N / 128);
+ * the last block of each dimension may be partial.
+ *
+ * fp8_quant_per_token_group:  x_bf16 [M, K] (ld ldx) -> xq [M, K] (ld ldq),
+ *   s_x [M, KB] fp32 row-major.  Requirements as for fp8_quant_per_token.
+ * fp8_quant_weight_blocks:    w_bf16 [N, K] (ld ldw) -> wq [N, K] (ld ldwq),
+ *   s_w [NB, KB] fp32 row-major (offline, once per checkpoint).  Same
+ *   requirements; NB <= 65535.
+ */
+FP8_API fp8_status_t fp8_quant_per_token_group(const void* x_bf16, int64_t M, int64_t K,
+                                               int64_t ldx, uint8_t* xq, int64_t ldq, float* s_x,
+                                               void* stream);
+FP8_API fp8_status_t fp8_quant_weight_blocks(const void* w_bf16, int64_t N, int64_t K,
+                                             int64_t ldw, uint8_t* wq, int64_t ldwq, float* s_w,
+                                             void* stream);
+
+/*
+ * Block-scaled GEMM:
+ *   y[m,n] = bf16_rn( sum_kb s_x[m,kb] * s_w[n/128,kb] *
+ *                     sum_{k in block kb} e4m3(xq[m,k]) * e4m3(wq[n,k]) )
+ * with each block's partial sum accumulated in fp32.
+ *
+ *   xq [device] E4M3 [M, K] contiguous; s_x fp32 [M, KB]
+ *   wq [device] E4M3 [N, K] contiguous; s_w fp32 [NB, KB]
+ *   y  [device, out] bf16 [M, N] contiguous
+ *   workspace  unused (may be NULL)
+ * Requirements as for fp8_scaled_gemm.
+ */
+FP8_API fp8_status_t fp8_scaled_gemm_blockwise(const uint8_t* xq, const float* s_x,
+                                               const uint8_t* wq, const float* s_w, void* y_bf16,
+                                               int64_t M, int64_t N, int64_t K, void* workspace,
+                                               size_t ws_bytes, void* stream);
+
+/*
+ * The block-scaled layer: group quantization of x (into the workspace: codes
+ * [M, K] at offset 0, s_x [M, KB] at round_up(M*K, 256)) followed by the
+ * block-scaled GEMM.  wq / s_w come from fp8_quant_weight_blocks.
+ * Requirements as for fp8_linear, with
+ * fp8_linear_blockwise_workspace_size(M, N, K) workspace bytes.
+ */
+FP8_API fp8_status_t fp8_linear_blockwise(const void* x_bf16, const uint8_t* wq, const float* s_w,
+                                          void* y_bf16, int64_t M, int64_t N, int64_t K,
+                                          void* workspace, size_t ws_bytes, void* stream);
+
+/* round_up(M*K, 256) + round_up(4*M*KB, 256) bytes. */
+FP8_API size_t fp8_linear_blockwise_workspace_size(int64_t M, int64_t N, int64_t K);
+
 /* Workspace bytes fp8_linear needs for an [M, K] x [N, K]^T layer:
  * round_up(M*K, 256) + round_up(4*M, 256).  0 for invalid sizes. */
 FP8_API size_t fp8_linear_workspace_size(int64_t M, int64_t N, int64_t K);

@@ -124,3 +124,23 @@ def test_host_checks_of_the_scale_variants(L):
     assert L.fp8_kv_cache_quant(fake, 4, 8, 128, fake + 2, 1, None, fake, 16, None) == UNSUP
     assert L.fp8_kv_cache_quant(fake, 0, 8, 128, fake, 1, None, fake, 16, None) == 0
     assert L.fp8_kv_cache_quant(fake, 4, 8, 128, fake, 1, None, fake, 0, None) == 0
+
+
+def test_host_checks_of_the_blockwise_calls(L):
+    INVALID, UNSUP, WS = 1, 2, 3
+    fake = 1 << 20
+    assert L.fp8_linear_blockwise_workspace_size(3, 7, 300) == 1024 + 256
+    assert L.fp8_linear_blockwise_workspace_size(1, 4096, 4096) == 4096 + 256
+    assert L.fp8_linear_blockwise_workspace_size(-1, 4, 32) == 0
+    assert L.fp8_quant_per_token_group(fake, 4, 24, 24, fake, 32, fake, None) == UNSUP
+    assert L.fp8_quant_per_token_group(fake, 4, 32, 32, fake, 32, None, None) == INVALID
+    assert L.fp8_quant_per_token_group(fake, 0, 32, 32, fake, 32, fake, None) == 0
+    assert L.fp8_quant_weight_blocks(fake, 65535 * 128 + 1, 32, 32, fake, 32, fake, None) == UNSUP
+    assert L.fp8_quant_weight_blocks(fake, 4, 32, 16, fake, 32, fake, None) == INVALID
+    assert L.fp8_scaled_gemm_blockwise(None, fake, fake, fake, fake, 4, 4, 32, None, 0, None) == INVALID
+    assert L.fp8_scaled_gemm_blockwise(fake, fake, fake, fake, fake, 4, 4, 40, None, 0, None) == UNSUP
+    assert L.fp8_scaled_gemm_blockwise(fake, fake, fake, fake, fake, 0, 4, 32, None, 0, None) == 0
+    assert L.fp8_linear_blockwise(fake, fake, fake, fake, 4, 4, 32, None, 0, None) == WS
+    assert L.fp8_linear_blockwise(fake, fake, fake, fake, 4, 4, 32, fake, 300, None) == WS
+    assert L.fp8_linear_blockwise(fake, fake, fake, fake, 4, 4, 20, fake, 4096, None) == UNSUP
+    assert L.fp8_linear_blockwise(fake, None, fake, fake, 4, 4, 32, fake, 4096, None) == INVALID
