@@ -367,6 +367,8 @@ def run_ours(args):
     del pxs, pys, pws
 
     variants = variant_rates(pkg, workloads, dev, stream, timed, hbm_peak, args.steps)
+    blockwise = blockwise_rates(pkg, workloads, dev, stream, timed, hbm_peak, fp8_peak,
+                                args.steps, l2)
 
     # --- e2e: public API with pinned host buffers, copies in the timed region
     hx = [x.cpu().pin_memory() for x in xs]
@@ -416,12 +418,93 @@ def run_ours(args):
             "roofline": roofline,
             "prefill": prefill,
             "scale_variants": variants,
+            "blockwise": blockwise,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
     return 0
+
+
+def blockwise_layer_bytes(M, K, N):
+    """Algorithmic bytes of a block-scaled decode layer: bf16 X in, E4M3 W and
+    its 128x128 block scales, bf16 Y out."""
+    kb, nb = -(-K // 128), -(-N // 128)
+    return 2 * M * K + N * K + 4 * nb * kb + 2 * M * N
+
+
+def blockwise_rates(pkg, workloads, dev, stream, timed, hbm_peak, fp8_peak, steps, l2):
+    """The block-scaled layer (1x128 activation groups, 128x128 weight blocks)
+    on the same decode step (CUDA graph per weight set, sets > 2 x L2) and the
+    same prefill layers as the per-channel path."""
+    import torch
+
+    calls = decode_calls()
+    per_set = sum(N * K for (_, K, N) in workloads.SHAPES_8B)
+    nsets = max(2, -(-2 * l2 // per_set) + 1)
+    wsets = []
+    for s_ in range(nsets):
+        d = {}
+        for (_, K, N) in workloads.SHAPES_8B:
+            w = workloads.weights(N, K, workloads.SEED_DECODE + 100 * s_, dev)
+            d[(K, N)] = pkg.fp8_quant_weight_blocks(w)
+            del w
+        wsets.append(d)
+    xs = [workloads.gaussian_outliers(M, K, workloads.SEED_DECODE, dev) for (M, K, N) in calls]
+    ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for (M, K, N) in calls]
+    wss = [torch.empty(pkg.fp8_linear_blockwise_workspace_size(M, N, K), dtype=torch.uint8,
+                       device=dev) for (M, K, N) in calls]
+    torch.cuda.synchronize()
+
+    def step(wset, st):
+        for i, (M, K, N) in enumerate(calls):
+            wq, sw = wset[(K, N)]
+            pkg.fp8_linear_blockwise(xs[i], wq, sw, y=ys[i], workspace=wss[i], stream=st)
+
+    graphs = []
+    with torch.cuda.stream(stream):
+        for wset in wsets:
+            step(wset, stream)
+        stream.synchronize()
+        for wset in wsets:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(wset, torch.cuda.current_stream())
+            graphs.append(g)
+    torch.cuda.synchronize()
+    n = max(steps, 50)
+    t = timed(lambda i: graphs[i % nsets].replay(), n, 3)
+    nbytes = sum(blockwise_layer_bytes(M, K, N) for (M, K, N) in calls)
+    gbs = nbytes * n / t / 1e9
+    decode = {"gbs": gbs, "frac": gbs / hbm_peak, "ms_per_step": t / n * 1e3,
+              "workload": "the decode step above (12 fp8_linear_blockwise calls)"}
+    del graphs, xs, ys, wss
+
+    pre_calls = [(M, K, N) for M in workloads.PREFILL_M for (_, K, N) in workloads.SHAPES_8B]
+    pxs = {}
+    for (M, K, N) in pre_calls:
+        if (M, K) not in pxs:
+            pxs[(M, K)] = workloads.student_t_outliers(M, K, workloads.SEED_PREFILL, dev)
+    pys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for (M, K, N) in pre_calls]
+    pws = torch.empty(max(pkg.fp8_linear_blockwise_workspace_size(M, N, K)
+                          for (M, K, N) in pre_calls), dtype=torch.uint8, device=dev)
+
+    def prefill_step(i):
+        for j, (M, K, N) in enumerate(pre_calls):
+            wq, sw = wsets[0][(K, N)]
+            pkg.fp8_linear_blockwise(pxs[(M, K)], wq, sw, y=pys[j], workspace=pws, stream=stream)
+
+    psteps = max(3, min(steps, 20))
+    t = timed(prefill_step, psteps, 2)
+    tflops = sum(2 * M * N * K for (M, K, N) in pre_calls) * psteps / t / 1e12
+    prefill = {"tflops": tflops, "frac": tflops / fp8_peak,
+               "workload": "llama-3.1-8b prefill layers, M in {2048,8192}, 8 calls"}
+    del pxs, pys, pws, wsets
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return {"decode": decode, "prefill": prefill,
+            "launches_per_decode_step": 2 * len(calls)}
 
 
 def variant_rates(pkg, workloads, dev, stream, timed, hbm_peak, steps):
@@ -502,6 +585,23 @@ def run_case(spec: str, reps: int = 4):
     kind, *dims = spec.split(",")
     if kind in ("static", "tensor", "kv"):
         return run_variant_case(pkg, workloads, dev, kind, [int(v) for v in dims], reps)
+    if kind == "block":
+        M, K, N = (int(v) for v in dims)
+        w = workloads.weights(N, K, workloads.SEED_DECODE, dev)
+        wq, s_w = pkg.fp8_quant_weight_blocks(w)
+        del w
+        x = workloads.student_t_outliers(M, K, workloads.SEED_PREFILL, dev)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(pkg.fp8_linear_blockwise_workspace_size(M, N, K), dtype=torch.uint8,
+                         device=dev)
+        torch.cuda.synchronize()
+        for _ in range(reps):
+            pkg.fp8_linear_blockwise(x, wq, s_w, y=y, workspace=ws)
+        torch.cuda.synchronize()
+        if pkg.fp8_device_status() != pkg.FP8_OK:
+            raise RuntimeError("a kernel gave up a bounded wait")
+        print(json.dumps({"case": ["block", M, K, N], "reps": reps, "ok": True}))
+        return 0
     M, K, N = (int(v) for v in spec.split(","))
     w = workloads.weights(N, K, workloads.SEED_DECODE, dev)
     wq, s_w = pkg.fp8_quant_per_channel_weights(w)
@@ -559,7 +659,8 @@ def main():
                     help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--case", default=None,
                     help="M,K,N: run fp8_linear on that one layer a few times and exit; "
-                         "static,M,K / tensor,M,K / kv,T,H,D: one quantizer variant")
+                         "static,M,K / tensor,M,K / kv,T,H,D: one quantizer variant; "
+                         "block,M,K,N: fp8_linear_blockwise on one layer")
     args = ap.parse_args()
     if args.case:
         return run_case(args.case)

@@ -11,11 +11,14 @@
 // (per-token scales; saturating conversion).
 //
 // Layout of the work: a group of G threads owns a row; each thread keeps up
-// to 4 16-element chunks (two 16-byte loads each) of the row in registers
+// to VPT 16-element chunks (two 16-byte loads each) of the row in registers
 // between the amax pass and the quantize pass, so X is read from HBM once.
 // The amax reduction is a butterfly of warp shuffles, then (G > 32) a pass
 // through shared memory.  Codes leave as one 16-byte store per chunk.
-// Very long rows (K > 65536) take a variant that streams the row twice.
+// Small problems (decode batches) use one chunk per thread, so each
+// thread's serial work -- the latency of the call -- is as short as
+// possible; large ones use four, so fewer threads carry the stream.  Very
+// long rows (K > 65536) take a variant that streams the row twice.
 //
 // Memory-bound: 2 bytes in + 1 byte out per element (+4 bytes per row).
 // Divisions use __fdiv_rn (IEEE round-to-nearest); nothing here is compiled
@@ -33,7 +36,10 @@ namespace fp8k {
 namespace {
 
 constexpr int kBlock = 256;  // threads per CTA for G <= 256
-constexpr int kVPT = 4;      // 16-element chunks per thread (register path)
+constexpr int kVPT = 4;      // 16-element chunks per thread, large problems
+// Total 16-element chunks up to which the one-chunk-per-thread (latency)
+// layout is used: about one wave of 1024 threads per SM on 152 SMs.
+constexpr int64_t kLatencyChunks = 152 * 1024;
 
 // Read-once 16-byte load that does not allocate in L1.
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
@@ -62,7 +68,7 @@ __device__ __forceinline__ float group_max(float m, float* red) {
     return m;
 }
 
-template <int G>
+template <int G, int VPT>
 __global__ void __launch_bounds__(G > kBlock ? G : kBlock)
     quant_rows_regs(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx,
                     uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s) {
@@ -82,10 +88,10 @@ __global__ void __launch_bounds__(G > kBlock ? G : kBlock)
     const int64_t C = K >> 4;  // 16-element chunks per row
 
     const uint4* xr = reinterpret_cast<const uint4*>(x + (live ? row : 0) * ldx);
-    uint4 v[kVPT][2];
+    uint4 v[VPT][2];
     float m = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kVPT; ++i) {
+    for (int i = 0; i < VPT; ++i) {
         const int64_t c = t + static_cast<int64_t>(i) * G;
         if (live && c < C) {
             v[i][0] = ld_stream(xr + 2 * c);
@@ -98,7 +104,7 @@ __global__ void __launch_bounds__(G > kBlock ? G : kBlock)
     if (!live) return;
     uint4* qr = reinterpret_cast<uint4*>(q + row * ldq);
 #pragma unroll
-    for (int i = 0; i < kVPT; ++i) {
+    for (int i = 0; i < VPT; ++i) {
         const int64_t c = t + static_cast<int64_t>(i) * G;
         if (c < C) {
             const uint2 a = quant8(v[i][0], sc);
@@ -164,13 +170,13 @@ cudaError_t launch_pdl(void (*kernel)(Params...), int64_t grid, int block, cudaS
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-template <int G>
+template <int G, int VPT>
 cudaError_t launch_regs(const uint16_t* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q,
                         int64_t ldq, float* s, cudaStream_t st) {
     constexpr int B = G > kBlock ? G : kBlock;
     constexpr int ROWS = B / G;
     const int64_t grid = (R + ROWS - 1) / ROWS;
-    return launch_pdl(quant_rows_regs<G>, grid, B, st, x, R, K, ldx, q, ldq, s);
+    return launch_pdl(quant_rows_regs<G, VPT>, grid, B, st, x, R, K, ldx, q, ldq, s);
 }
 
 }  // namespace
@@ -182,12 +188,21 @@ cudaError_t launch_quant_rows(const void* x, int64_t R, int64_t K, int64_t ldx, 
     const uint16_t* xb = static_cast<const uint16_t*>(x);
     if (K == 0) return launch_pdl(fill_ones, (R + 255) / 256, 256, st, s, R);
     const int64_t C = K / 16;
-    if (C <= 32 * kVPT) return launch_regs<32>(xb, R, K, ldx, q, ldq, s, st);
-    if (C <= 64 * kVPT) return launch_regs<64>(xb, R, K, ldx, q, ldq, s, st);
-    if (C <= 128 * kVPT) return launch_regs<128>(xb, R, K, ldx, q, ldq, s, st);
-    if (C <= 256 * kVPT) return launch_regs<256>(xb, R, K, ldx, q, ldq, s, st);
-    if (C <= 512 * kVPT) return launch_regs<512>(xb, R, K, ldx, q, ldq, s, st);
-    if (C <= 1024 * kVPT) return launch_regs<1024>(xb, R, K, ldx, q, ldq, s, st);
+    if (R * C <= kLatencyChunks) {
+        if (C <= 32) return launch_regs<32, 1>(xb, R, K, ldx, q, ldq, s, st);
+        if (C <= 64) return launch_regs<64, 1>(xb, R, K, ldx, q, ldq, s, st);
+        if (C <= 128) return launch_regs<128, 1>(xb, R, K, ldx, q, ldq, s, st);
+        if (C <= 256) return launch_regs<256, 1>(xb, R, K, ldx, q, ldq, s, st);
+        if (C <= 512) return launch_regs<512, 1>(xb, R, K, ldx, q, ldq, s, st);
+        if (C <= 1024) return launch_regs<1024, 1>(xb, R, K, ldx, q, ldq, s, st);
+        if (C <= 2048) return launch_regs<1024, 2>(xb, R, K, ldx, q, ldq, s, st);
+    }
+    if (C <= 32 * kVPT) return launch_regs<32, kVPT>(xb, R, K, ldx, q, ldq, s, st);
+    if (C <= 64 * kVPT) return launch_regs<64, kVPT>(xb, R, K, ldx, q, ldq, s, st);
+    if (C <= 128 * kVPT) return launch_regs<128, kVPT>(xb, R, K, ldx, q, ldq, s, st);
+    if (C <= 256 * kVPT) return launch_regs<256, kVPT>(xb, R, K, ldx, q, ldq, s, st);
+    if (C <= 512 * kVPT) return launch_regs<512, kVPT>(xb, R, K, ldx, q, ldq, s, st);
+    if (C <= 1024 * kVPT) return launch_regs<1024, kVPT>(xb, R, K, ldx, q, ldq, s, st);
     return launch_pdl(quant_rows_stream, R, 1024, st, xb, R, K, ldx, q, ldq, s);
 }
 
