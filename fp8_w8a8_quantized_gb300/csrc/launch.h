@@ -42,6 +42,11 @@ bool encode_tmap_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 // Persistent 128x256-tile tcgen05 GEMM for large M (gemm_prefill.cu).
 cudaError_t launch_gemm_prefill(const GemmArgs& a);
 
+// Persistent 256x256-tile GEMM on pairs of SMs (tcgen05 cta_group::2) for
+// M >= kPairMinM (gemm_pair.cu).
+constexpr int kPairMinM = 256;
+cudaError_t launch_gemm_pair(const GemmArgs& a);
+
 // Weight-streaming split-K tcgen05 GEMM for M <= 64 (gemm_decode.cu).
 constexpr int kDecodeMaxM = 64;
 cudaError_t launch_gemm_decode(const GemmArgs& a);
@@ -78,5 +83,6 @@ cudaError_t launch_gemm_blockwise(const GemmArgs& a);
 cudaError_t prepare_gemm_prefill();
 cudaError_t prepare_gemm_decode();
 cudaError_t prepare_gemm_blockwise();
+cudaError_t prepare_gemm_pair();
 
 }  // namespace fp8k

@@ -1,6 +1,7 @@
-"""GPU parity of the scaled FP8 GEMM (both kernels: the weight-streaming
-split-K kernel for M <= 64 and the persistent tile kernel above), fed with the
-oracle's own codes and scales, against the oracle's fp64 result."""
+"""GPU parity of the scaled FP8 GEMM (all three kernels: the weight-streaming
+split-K kernel for M <= 64, the one-SM persistent tile kernel up to M = 255
+and the paired-SM 256 x 256 tile kernel above), fed with the oracle's own
+codes and scales, against the oracle's fp64 result."""
 import numpy as np
 import pytest
 import torch
@@ -37,6 +38,7 @@ SHAPES = [  # (M, N, K): ragged edges, single k-block, many k-blocks, both kerne
     (1, 8, 16), (1, 128, 128), (3, 24, 48), (16, 256, 256), (17, 100, 272), (32, 264, 1024),
     (33, 1000, 4096), (64, 384, 2048), (65, 256, 256), (128, 256, 128), (129, 520, 1040),
     (200, 300, 4112), (256, 512, 4096), (300, 1000, 1024), (513, 777, 2064),
+    (256, 256, 128), (257, 264, 256), (1000, 4100, 512), (2048, 520, 272), (384, 128, 8192),
 ]
 
 
