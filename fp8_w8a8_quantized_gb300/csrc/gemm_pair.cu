@@ -8,15 +8,18 @@
 // Works at the Hardware Level"), with a 256 x 256 output tile per cluster of
 // two CTAs on two SMs.  One MMA instruction (M = 256, N = 256, K = 32) runs on
 // both SMs' tensor cores: each CTA holds its own 128 rows of the activation
-// tile and half of the weight tile, so per SM and per 128-deep k-block TMA
-// writes 32 KB into shared memory instead of the 48 KB a one-SM 128 x 256
-// tile needs, for the same number of MMA flops per SM -- the one-SM kernel is
-// bound by shared-memory traffic (TMA writes plus tensor-core operand reads).
+// tile and half of the weight tile, so per SM and per 128 of K, TMA writes
+// 32 KB into shared memory instead of the 48 KB a one-SM 128 x 256 tile
+// needs, for the same number of MMA flops per SM.  A ring stage holds 256 of
+// K (two 128-byte swizzle columns per operand), so each barrier round trip
+// and each commit covers eight MMAs: per-stage overhead, not bandwidth, was
+// what held the tensor pipe back with 128-deep stages (measured on GB300).
 //
 // Per CTA (192 threads):
 //   warp 0      TMA producer: its 128 activation rows and 128 weight rows of
-//               each k-block into a 6-stage ring; completion is counted on
-//               the even CTA's barrier (cta_group::2 TMA);
+//               each 256-deep k-block into a 3-stage ring (64 KB a stage);
+//               completion is counted on the even CTA's barrier (cta_group::2
+//               TMA);
 //   warp 1      allocates the pair's TMEM (collectively with the peer); in the
 //               even CTA it issues the pair MMAs and multicasts each commit to
 //               both CTAs' barriers;
@@ -37,9 +40,10 @@ namespace {
 
 constexpr int BM = 256;      // output rows per pair (128 per CTA)
 constexpr int BN = 256;      // output columns per pair (B split 128 / 128)
-constexpr int BK = 128;      // bytes of K per stage
+constexpr int BK = 256;      // bytes of K per stage (two 128-byte swizzle columns)
+constexpr int BKS = 128;     // bytes of K per swizzle column / TMA box
 constexpr int KSTEP = 32;    // K of one tcgen05.mma kind::f8f6f4
-constexpr int STAGES = 6;
+constexpr int STAGES = 3;
 constexpr int kGroupM = 8;   // row-block groups for L2 reuse of weight tiles
 constexpr int kThreads = 192;
 constexpr int kAccBufs = 2;  // TMEM accumulator buffers of BN columns
@@ -140,13 +144,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int a_row = m_blk * BM + static_cast<int>(rank) * (BM / 2);
             const int b_row = n_blk * BN + static_cast<int>(rank) * (BN / 2);
             for (int kb = 0; kb < nk; ++kb) {
-                if (!(ok = warp_wait_cluster(&bars->empty[stage], phase ^ 1u, abort_flag, status)))
-                    break;
+                if (!(ok = warp_wait(&bars->empty[stage], phase ^ 1u, abort_flag, status))) break;
                 if (lane == 0) {
                     const uint32_t full0 = map_to_rank(smem_u32(&bars->full[stage]), 0);
                     if (leader) mbar_arrive_expect_tx(&bars->full[stage], 2 * STAGE_BYTES);
-                    tma_load_2d_pair(sA + stage * A_TILE, &tmA, full0, kb * BK, a_row);
-                    tma_load_2d_pair(sB + stage * B_TILE, &tmB, full0, kb * BK, b_row);
+#pragma unroll
+                    for (int j = 0; j < BK / BKS; ++j) {
+                        tma_load_2d_pair(sA + stage * A_TILE + j * (A_TILE / 2), &tmA, full0,
+                                         kb * BK + j * BKS, a_row);
+                        tma_load_2d_pair(sB + stage * B_TILE + j * (B_TILE / 2), &tmB, full0,
+                                         kb * BK + j * BKS, b_row);
+                    }
                 }
                 __syncwarp();
                 if (++stage == STAGES) {
@@ -171,15 +179,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * BN;
                 for (int kb = 0; kb < nk; ++kb) {
-                    if (!(ok = warp_wait_cluster(&bars->full[stage], phase, abort_flag, status)))
-                        break;
+                    if (!(ok = warp_wait(&bars->full[stage], phase, abort_flag, status))) break;
                     tc_fence_after();
                     if (lane == 0) {
                         const uint64_t a0 = sdesc_kmajor_sw128(smem_u32(sA + stage * A_TILE));
                         const uint64_t b0 = sdesc_kmajor_sw128(smem_u32(sB + stage * B_TILE));
 #pragma unroll
-                        for (int kk = 0; kk < BK / KSTEP; ++kk)
-                            mma_f8_pair(d_tmem, a0 + 2 * kk, b0 + 2 * kk, idesc, (kb | kk) != 0);
+                        for (int kk = 0; kk < BK / KSTEP; ++kk) {
+                            const int j = kk / (BKS / KSTEP), w = kk % (BKS / KSTEP);
+                            mma_f8_pair(d_tmem, a0 + ((j * (A_TILE / 2)) >> 4) + 2 * w,
+                                        b0 + ((j * (B_TILE / 2)) >> 4) + 2 * w, idesc,
+                                        (kb | kk) != 0);
+                        }
                         mma_commit_pair(&bars->empty[stage], 0x3);
                     }
                     __syncwarp();
@@ -210,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tile_coords(t, num_m, num_n, m_blk, n_blk);
             const int buf = local % kAccBufs;
             const uint32_t acc_phase = (local / kAccBufs) & 1;
-            if (!warp_wait_cluster(&bars->acc_full[buf], acc_phase, abort_flag, status)) break;
+            if (!warp_wait(&bars->acc_full[buf], acc_phase, abort_flag, status)) break;
             tc_fence_after();
             const int m = m_blk * BM + row_in_tile;
             const bool row_ok = m < M;
@@ -317,8 +328,8 @@ int co_resident_pairs(int num_sms) {
 
 cudaError_t launch_gemm_pair(const GemmArgs& a) {
     CUtensorMap tmA, tmB;
-    if (!encode_tmap_u8(&tmA, a.xq, a.M, a.K, a.K, BK, BM / 2)) return cudaErrorInvalidValue;
-    if (!encode_tmap_u8(&tmB, a.wq, a.N, a.K, a.K, BK, BN / 2)) return cudaErrorInvalidValue;
+    if (!encode_tmap_u8(&tmA, a.xq, a.M, a.K, a.K, BKS, BM / 2)) return cudaErrorInvalidValue;
+    if (!encode_tmap_u8(&tmB, a.wq, a.N, a.K, a.K, BKS, BN / 2)) return cudaErrorInvalidValue;
     const int tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
     const int max_pairs = co_resident_pairs(a.num_sms);
     const int pairs = tiles < max_pairs ? tiles : max_pairs;
