@@ -98,6 +98,11 @@ def _load():
         lib.orc_gemm_blockwise.restype = None
         lib.orc_gemm_blockwise.argtypes = [_vp, _i64, _vp, _vp, _i64, _vp, _i64, _i64, _i64,
                                            _i64, _i64, _i64, _vp, _vp, _vp]
+        lib.orc_rmsnorm_bracket_bf16.restype = None
+        lib.orc_rmsnorm_bracket_bf16.argtypes = [_vp, _i64, _i64, _i64, _vp, ctypes.c_float,
+                                                 ctypes.c_double, _vp, _vp, _vp]
+        lib.orc_rmsnorm_f64.restype = None
+        lib.orc_rmsnorm_f64.argtypes = [_vp, _i64, _i64, _i64, _vp, ctypes.c_double, _vp]
         lib.orc_num_threads.restype = ctypes.c_int
         lib.orc_num_threads.argtypes = []
         _lib = lib
@@ -347,4 +352,39 @@ def gemm_blockwise(qx, s_x, qw, s_w, bn: int = GROUP, bk: int = GROUP,
     if r.size:
         lib.orc_gemm_blockwise(_ptr(a), K, _ptr(sx), _ptr(b), K, _ptr(sw), M, N, K, bn, bk,
                                r.size, _ptr(r), _ptr(c), _ptr(y))
+    return y
+
+
+# --------------------------------------------------------------------------
+# RMSNorm -> per-token quantization
+# --------------------------------------------------------------------------
+
+def rmsnorm_bracket_bf16(x_bits: np.ndarray, g_bits: np.ndarray, eps: float, rel_err: float):
+    """bf16 RMSNorm of every row under the fp32 reading, bracketed for a sum
+    of squares known to relative rel_err: returns (y_lo, y_hi, ss) where y_lo
+    / y_hi are bf16 bits [R, K] (equal wherever the sum's error cannot change
+    the rounding) and ss the exact sums of squares (fp64)."""
+    lib = _load()
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    g = np.ascontiguousarray(g_bits, dtype=np.uint16)
+    R, K = x.shape
+    assert g.shape == (K,)
+    y_lo = np.zeros((R, K), dtype=np.uint16)
+    y_hi = np.zeros((R, K), dtype=np.uint16)
+    ss = np.zeros(R, dtype=np.float64)
+    if R and K:
+        lib.orc_rmsnorm_bracket_bf16(_ptr(x), R, K, K, _ptr(g), float(eps), float(rel_err),
+                                     _ptr(y_lo), _ptr(y_hi), _ptr(ss))
+    return y_lo, y_hi, ss
+
+
+def rmsnorm_f64(x_bits: np.ndarray, g_bits: np.ndarray, eps: float) -> np.ndarray:
+    """The real normalised values (fp64, no intermediate rounding)."""
+    lib = _load()
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    g = np.ascontiguousarray(g_bits, dtype=np.uint16)
+    R, K = x.shape
+    y = np.zeros((R, K), dtype=np.float64)
+    if R and K:
+        lib.orc_rmsnorm_f64(_ptr(x), R, K, K, _ptr(g), float(eps), _ptr(y))
     return y

@@ -441,3 +441,94 @@ void orc_gemm_blockwise(const uint8_t* qx, int64_t ldqx, const float* s_x,
         y[p] = acc;
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* RMSNorm feeding the per-token quantizer (the amax reduction fused into     */
+/* the preceding kernel)                                                      */
+/* ------------------------------------------------------------------------ */
+
+static uint16_t f32_to_bf16_rn(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u)
+        return (uint16_t)((u >> 16) | 0x40);            /* quiet NaN */
+    u += 0x7FFFu + ((u >> 16) & 1u);                     /* round to nearest even */
+    return (uint16_t)(u >> 16);
+}
+
+/* The normalisation of one row, given its sum of squares ss, as the fp32
+ * steps of the reading: mean = fl32(ss / K); r = fl32(sqrt(fl32(mean + eps)));
+ * inv = fl32(1 / r); y_k = bf16(fl32(fl32(x_k * inv) * g_k)).  Every step is
+ * monotone in ss, so y at two sums brackets y at any sum between them. */
+static void rms_row_from_ss(const uint16_t* x, const uint16_t* g, int64_t K, float eps,
+                            float ss, uint16_t* y)
+{
+    volatile float mean = ss / (float)K;
+    volatile float t = mean + eps;
+    volatile float r = sqrtf(t);
+    volatile float inv = 1.0f / r;
+    int64_t k;
+    for (k = 0; k < K; ++k) {
+        volatile float a = bf16_to_f32(x[k]) * inv;
+        volatile float b = a * bf16_to_f32(g[k]);
+        y[k] = f32_to_bf16_rn(b);
+    }
+}
+
+/* RMSNorm (y = x / sqrt(mean(x^2) + eps) * g, "FP8 Inference Explained, in
+ * depth", "What stays in higher precision": normalisation stays in 16- or
+ * 32-bit, and "Scales and their granularity": the amax reduction is fused
+ * into the preceding kernel).  The sum of squares is exact here (fp64 sums of
+ * bf16 squares, each exact) and the GPU's fp32 sum lies within a relative
+ * rel_err of it, so the row is evaluated at ss * (1 - rel_err) and
+ * ss * (1 + rel_err) (rounded outwards to fp32): y_lo / y_hi bracket every
+ * bf16 value the GPU may produce, element by element.  ss_out is the exact
+ * sum. */
+void orc_rmsnorm_bracket_bf16(const uint16_t* x, int64_t R, int64_t K, int64_t ldx,
+                              const uint16_t* g, float eps, double rel_err,
+                              uint16_t* y_lo, uint16_t* y_hi, double* ss_out)
+{
+    int64_t r;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (r = 0; r < R; ++r) {
+        const uint16_t* xr = x + r * ldx;
+        double ss = 0.0, lo, hi;
+        float flo, fhi;
+        int64_t k;
+        for (k = 0; k < K; ++k) {
+            double v = (double)bf16_to_f32(xr[k]);
+            ss += v * v;
+        }
+        lo = ss * (1.0 - rel_err);
+        hi = ss * (1.0 + rel_err);
+        flo = (float)lo;
+        if ((double)flo > lo)
+            flo = nextafterf(flo, 0.0f);
+        fhi = (float)hi;
+        if ((double)fhi < hi)
+            fhi = nextafterf(fhi, INFINITY);
+        /* a larger sum gives a smaller |y| */
+        rms_row_from_ss(xr, g, K, eps, fhi, y_lo + r * K);
+        rms_row_from_ss(xr, g, K, eps, flo, y_hi + r * K);
+        ss_out[r] = ss;
+    }
+}
+
+/* The same steps in fp64 throughout (no intermediate rounding): the real
+ * normalised values, for comparison with an independent library routine. */
+void orc_rmsnorm_f64(const uint16_t* x, int64_t R, int64_t K, int64_t ldx, const uint16_t* g,
+                     double eps, double* y)
+{
+    int64_t r, k;
+    for (r = 0; r < R; ++r) {
+        double ss = 0.0, inv;
+        for (k = 0; k < K; ++k) {
+            double v = (double)bf16_to_f32(x[r * ldx + k]);
+            ss += v * v;
+        }
+        inv = 1.0 / sqrt(ss / (double)K + eps);
+        for (k = 0; k < K; ++k)
+            y[r * K + k] = (double)bf16_to_f32(x[r * ldx + k]) * inv * (double)bf16_to_f32(g[k]);
+    }
+}
