@@ -541,7 +541,23 @@ def variant_rates(pkg, workloads, dev, stream, timed, hbm_peak, steps):
               n, 3)
     out["per_tensor"] = dict(rate(t, act_bytes), workload=f"{M}x{K} bf16", launches=2,
                              note="two passes over x; the second mostly hits L2")
-    del xs, qs
+    # RMSNorm with the quantizer fused in, against RMSNorm written to bf16
+    # (torch, a library kernel: context only) followed by the quantizer
+    gam = (1.0 + 0.1 * torch.randn(K, device=dev)).to(torch.bfloat16)
+    t = timed(lambda i: pkg.fp8_rmsnorm_quant(xs[i % nbuf], gam, 1e-6, xq=qs[i % nbuf],
+                                              s_tok=s_rows, stream=stream), n, 3)
+    out["rmsnorm_quant"] = dict(rate(t, act_bytes + 2 * K), workload=f"{M}x{K} bf16",
+                                launches=1)
+    ys = [torch.empty_like(xs[0]) for _ in range(nbuf)]
+
+    def unfused(i):
+        ys[i % nbuf] = torch.nn.functional.rms_norm(xs[i % nbuf], (K,), gam, 1e-6)
+        pkg.fp8_quant_per_token(ys[i % nbuf], xq=qs[i % nbuf], s_tok=s_rows, stream=stream)
+
+    t2 = timed(unfused, n, 3)
+    out["rmsnorm_quant"]["unfused_us_per_call"] = t2 / n * 1e6
+    out["rmsnorm_quant"]["unfused"] = "torch rms_norm to bf16, then fp8_quant_per_token"
+    del xs, qs, ys
 
     # KV-cache write: 8 KV heads x 128, one layer's keys (or values) of an
     # 8192-token prefill scattered into a paged cache, 16 layers rotated

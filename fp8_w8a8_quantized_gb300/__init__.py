@@ -15,12 +15,14 @@ from ._binding import (  # noqa: F401
     fp8_linear,
     fp8_linear_blockwise,
     fp8_linear_blockwise_workspace_size,
+    fp8_linear_rmsnorm,
     fp8_linear_workspace_size,
     fp8_quant_per_channel_weights,
     fp8_quant_per_tensor,
     fp8_quant_per_token,
     fp8_quant_per_token_group,
     fp8_quant_weight_blocks,
+    fp8_rmsnorm_quant,
     fp8_quant_static,
     fp8_scaled_gemm,
     fp8_scaled_gemm_blockwise,

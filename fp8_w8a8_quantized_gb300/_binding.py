@@ -86,6 +86,12 @@ def lib() -> ctypes.CDLL:
                                            ctypes.c_size_t, _vp]
         L.fp8_linear_blockwise_workspace_size.restype = ctypes.c_size_t
         L.fp8_linear_blockwise_workspace_size.argtypes = [_i64, _i64, _i64]
+        L.fp8_rmsnorm_quant.restype = _st
+        L.fp8_rmsnorm_quant.argtypes = [_vp, _vp, ctypes.c_float, _i64, _i64, _i64, _vp, _i64,
+                                        _vp, _vp, _vp]
+        L.fp8_linear_rmsnorm.restype = _st
+        L.fp8_linear_rmsnorm.argtypes = [_vp, _vp, ctypes.c_float, _vp, _vp, _vp, _i64, _i64,
+                                         _i64, _vp, ctypes.c_size_t, _vp]
         L.fp8_status_string.restype = ctypes.c_char_p
         L.fp8_status_string.argtypes = [_st]
         L.fp8_device_status.restype = _st
@@ -235,6 +241,45 @@ def fp8_kv_cache_quant(kv: torch.Tensor, scale: torch.Tensor, cache: torch.Tenso
                                     _ptr(cache), cache.shape[0], _stream(stream)),
            "fp8_kv_cache_quant")
     return cache
+
+
+def fp8_rmsnorm_quant(x: torch.Tensor, gamma: torch.Tensor, eps: float,
+                      xq: torch.Tensor | None = None, s_tok: torch.Tensor | None = None,
+                      y: torch.Tensor | bool | None = None, stream=None):
+    """RMSNorm of bf16 x [M, K] with weights gamma [K], quantized per token.
+    Returns (codes uint8 [M, K], fp32 scales [M], normalised bf16 rows or
+    None); pass y=True (or a bf16 [M, K] tensor) to get the rows."""
+    M, K, ldx = _rows(x, "x")
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if s_tok is None:
+        s_tok = torch.empty((M,), dtype=torch.float32, device=x.device)
+    if y is True:
+        y = torch.empty((M, K), dtype=torch.bfloat16, device=x.device)
+    elif y is False:
+        y = None
+    _check(lib().fp8_rmsnorm_quant(_ptr(x), _ptr(gamma), float(eps), M, K, ldx, _ptr(xq),
+                                   xq.stride(0) if M else K, _ptr(s_tok), _ptr(y),
+                                   _stream(stream)), "fp8_rmsnorm_quant")
+    return xq, s_tok, y
+
+
+def fp8_linear_rmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float, wq: torch.Tensor,
+                       s_w: torch.Tensor, y: torch.Tensor | None = None,
+                       workspace: torch.Tensor | None = None, stream=None):
+    """The layer fed by RMSNorm: y = fp8_linear(rms_norm(x) * gamma) with the
+    per-token quantization fused into the normalisation kernel."""
+    M, K = x.shape
+    N = wq.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    need = fp8_linear_workspace_size(M, N, K)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=x.device)
+    _check(lib().fp8_linear_rmsnorm(_ptr(x), _ptr(gamma), float(eps), _ptr(wq), _ptr(s_w),
+                                    _ptr(y), M, N, K, _ptr(workspace), workspace.numel(),
+                                    _stream(stream)), "fp8_linear_rmsnorm")
+    return y
 
 
 BLOCK = 128  # edge of the block-wise scales

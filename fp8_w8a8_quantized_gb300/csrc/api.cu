@@ -2,8 +2,8 @@
 //
 // This file only validates arguments on the host, keeps a little per-device
 // state (SM count, the device status word, kernel attributes) and launches
-// the kernels of quant.cu, quant_variants.cu, gemm_prefill.cu, gemm_pair.cu,
-// gemm_decode.cu and gemm_blockwise.cu.  It never
+// the kernels of quant.cu, quant_variants.cu, norm_quant.cu, gemm_prefill.cu,
+// gemm_pair.cu, gemm_decode.cu and gemm_blockwise.cu.  It never
 // allocates device memory and never synchronizes, except in
 // fp8_device_status().
 #include <cuda.h>
@@ -370,6 +370,49 @@ fp8_status_t fp8_linear_blockwise(const void* x_bf16, const uint8_t* wq, const f
     // as in fp8_linear: the quantizer releases the GEMM only after its own
     // wait, so the GEMM may stream weights before its griddepcontrol.wait
     return run_gemm(xq, s_x, wq, s_w, y_bf16, M, N, K, true, stream, d, true);
+}
+
+fp8_status_t fp8_rmsnorm_quant(const void* x_bf16, const void* gamma_bf16, float eps, int64_t M,
+                               int64_t K, int64_t ldx, uint8_t* xq, int64_t ldq, float* s_tok,
+                               void* y_bf16, void* stream) {
+    fp8_status_t st = check_quant(x_bf16, M, K, ldx, xq, ldq, s_tok);
+    if (st != FP8_OK || M == 0) return st;
+    if (K == 0 || K > 65536) return FP8_ERR_UNSUPPORTED;
+    if (!gamma_bf16) return FP8_ERR_INVALID_ARG;
+    if (!aligned(gamma_bf16, 16) || (y_bf16 && !aligned(y_bf16, 16))) return FP8_ERR_UNSUPPORTED;
+    if (!(eps >= 0.0f) || eps > 3.0e38f) return FP8_ERR_INVALID_ARG;
+    DeviceState* d = nullptr;
+    if ((st = current_device(&d)) != FP8_OK) return st;
+    cudaError_t e = fp8k::launch_rmsnorm_quant(x_bf16, gamma_bf16, eps, M, K, ldx, xq, ldq, s_tok,
+                                               y_bf16, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+fp8_status_t fp8_linear_rmsnorm(const void* x_bf16, const void* gamma_bf16, float eps,
+                                const uint8_t* wq, const float* s_w, void* y_bf16, int64_t M,
+                                int64_t N, int64_t K, void* workspace, size_t ws_bytes,
+                                void* stream) {
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return FP8_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return FP8_OK;
+    if (!x_bf16 || !gamma_bf16 || !wq || !s_w || !y_bf16) return FP8_ERR_INVALID_ARG;
+    if (K <= 0 || K % 16 != 0 || K > 65536) return FP8_ERR_UNSUPPORTED;
+    if (!aligned(x_bf16, 16) || !aligned(gamma_bf16, 16)) return FP8_ERR_UNSUPPORTED;
+    if (!(eps >= 0.0f) || eps > 3.0e38f) return FP8_ERR_INVALID_ARG;
+    const size_t need = fp8_linear_workspace_size(M, N, K);
+    if (!workspace || ws_bytes < need || !aligned(workspace, 256)) return FP8_ERR_WORKSPACE;
+    uint8_t* xq = static_cast<uint8_t*>(workspace);
+    float* s_tok = reinterpret_cast<float*>(xq + round_up(static_cast<size_t>(M) * K, 256));
+    fp8_status_t st = check_gemm(xq, s_tok, wq, s_w, y_bf16, M, N, K);
+    if (st != FP8_OK) return st;
+    DeviceState* d = nullptr;
+    if ((st = current_device(&d)) != FP8_OK) return st;
+    cudaError_t e = fp8k::launch_rmsnorm_quant(x_bf16, gamma_bf16, eps, M, K, K, xq, K, s_tok,
+                                               nullptr, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return FP8_ERR_CUDA;
+    // as in fp8_linear: the producer of the codes releases the GEMM only after
+    // its own wait, so the GEMM may stream weights before its wait
+    return run_gemm(xq, s_tok, wq, s_w, y_bf16, M, N, K, true, stream, d);
 }
 
 const char* fp8_status_string(fp8_status_t status) {

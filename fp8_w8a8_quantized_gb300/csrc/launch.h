@@ -67,6 +67,12 @@ cudaError_t launch_kv_cache_quant(const void* x, int64_t T, int64_t H, int64_t D
                                   const float* scale, int64_t scale_stride, const int64_t* slot,
                                   uint8_t* cache, int64_t n_slots, int num_sms, cudaStream_t st);
 
+// RMSNorm fused with the per-token quantizer (norm_quant.cu); K <= 65536.
+// y (optional) receives the bf16 normalised rows, [R, K] contiguous.
+cudaError_t launch_rmsnorm_quant(const void* x, const void* gamma, float eps, int64_t R,
+                                 int64_t K, int64_t ldx, uint8_t* q, int64_t ldq, float* s,
+                                 void* y, cudaStream_t st);
+
 // Block-wise scales (quant_variants.cu): activations one scale per token per
 // 128 inputs, s [R, ceil(K/128)]; weights one scale per 128 x 128 block,
 // s [ceil(N/128), ceil(K/128)].

@@ -292,6 +292,40 @@ FP8_API fp8_status_t fp8_linear_blockwise(const void* x_bf16, const uint8_t* wq,
 /* round_up(M*K, 256) + round_up(4*M*KB, 256) bytes. */
 FP8_API size_t fp8_linear_blockwise_workspace_size(int64_t M, int64_t N, int64_t K);
 
+/*
+ * RMSNorm with the per-token quantizer fused into it (the amax reduction done
+ * by the kernel that produces the activations).  Source: "FP8 Inference
+ * Explained, in depth", "Scales and their granularity" (engines fuse the
+ * per-token amax into the preceding kernel) and "What stays in higher
+ * precision" (normalisation stays in 16/32-bit).  The pages do not define the
+ * normalisation; this is RMSNorm with every step an IEEE fp32 operation:
+ *   ss = sum_k x_k^2 (fp32, within 2^-17 relative of the exact sum),
+ *   inv = fl32(1 / fl32(sqrt(fl32(fl32(ss / K) + eps)))),
+ *   y_k = bf16_rn(fl32(fl32(x_k * inv) * gamma_k)),
+ * followed by the per-token rule of fp8_quant_per_token on the bf16 row y.
+ *
+ *   x_bf16     [device, in]  bf16 [M, K], leading dimension ldx
+ *   gamma_bf16 [device, in]  bf16 [K], 16-byte aligned
+ *   eps                      >= 0, finite
+ *   xq, ldq, s_tok           as for fp8_quant_per_token (codes of y, scales)
+ *   y_bf16     [device, out] bf16 [M, K] contiguous, or NULL: the normalised
+ *                            rows the codes were taken from
+ * Requirements as for fp8_quant_per_token, and 0 < K <= 65536.
+ */
+FP8_API fp8_status_t fp8_rmsnorm_quant(const void* x_bf16, const void* gamma_bf16, float eps,
+                                       int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
+                                       int64_t ldq, float* s_tok, void* y_bf16, void* stream);
+
+/*
+ * The layer fed by RMSNorm: fp8_rmsnorm_quant of x into the workspace (the
+ * same layout and size as fp8_linear's) followed by the scaled GEMM.
+ * x contiguous [M, K]; requirements as for fp8_linear and K <= 65536.
+ */
+FP8_API fp8_status_t fp8_linear_rmsnorm(const void* x_bf16, const void* gamma_bf16, float eps,
+                                        const uint8_t* wq, const float* s_w, void* y_bf16,
+                                        int64_t M, int64_t N, int64_t K, void* workspace,
+                                        size_t ws_bytes, void* stream);
+
 /* Workspace bytes fp8_linear needs for an [M, K] x [N, K]^T layer:
  * round_up(M*K, 256) + round_up(4*M, 256).  0 for invalid sizes. */
 FP8_API size_t fp8_linear_workspace_size(int64_t M, int64_t N, int64_t K);

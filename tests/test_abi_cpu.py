@@ -144,3 +144,21 @@ def test_host_checks_of_the_blockwise_calls(L):
     assert L.fp8_linear_blockwise(fake, fake, fake, fake, 4, 4, 32, fake, 300, None) == WS
     assert L.fp8_linear_blockwise(fake, fake, fake, fake, 4, 4, 20, fake, 4096, None) == UNSUP
     assert L.fp8_linear_blockwise(fake, None, fake, fake, 4, 4, 32, fake, 4096, None) == INVALID
+
+
+def test_host_checks_of_the_rmsnorm_calls(L):
+    INVALID, UNSUP, WS = 1, 2, 3
+    fake = 1 << 20
+    # x, gamma, eps, M, K, ldx, xq, ldq, s_tok, y, stream
+    assert L.fp8_rmsnorm_quant(fake, None, 1e-6, 4, 32, 32, fake, 32, fake, None, None) == INVALID
+    assert L.fp8_rmsnorm_quant(fake, fake, -1.0, 4, 32, 32, fake, 32, fake, None, None) == INVALID
+    assert L.fp8_rmsnorm_quant(fake, fake, float("nan"), 4, 32, 32, fake, 32, fake, None, None) == INVALID
+    assert L.fp8_rmsnorm_quant(fake, fake + 8, 1e-6, 4, 32, 32, fake, 32, fake, None, None) == UNSUP
+    assert L.fp8_rmsnorm_quant(fake, fake, 1e-6, 4, 65552, 65552, fake, 65552, fake, None, None) == UNSUP
+    assert L.fp8_rmsnorm_quant(fake, fake, 1e-6, 4, 32, 32, fake, 32, fake, fake + 4, None) == UNSUP
+    assert L.fp8_rmsnorm_quant(fake, fake, 1e-6, 0, 32, 32, fake, 32, fake, None, None) == 0
+    # x, gamma, eps, wq, s_w, y, M, N, K, ws, ws_bytes, stream
+    assert L.fp8_linear_rmsnorm(fake, fake, 1e-6, fake, fake, fake, 4, 4, 32, None, 0, None) == WS
+    assert L.fp8_linear_rmsnorm(fake, None, 1e-6, fake, fake, fake, 4, 4, 32, fake, 4096, None) == INVALID
+    assert L.fp8_linear_rmsnorm(fake, fake, 1e-6, fake, fake, fake, 4, 4, 24, fake, 4096, None) == UNSUP
+    assert L.fp8_linear_rmsnorm(fake, fake, 1e-6, fake, fake, fake, 0, 4, 32, None, 0, None) == 0
