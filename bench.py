@@ -370,26 +370,40 @@ def run_ours(args):
     blockwise = blockwise_rates(pkg, workloads, dev, stream, timed, hbm_peak, fp8_peak,
                                 args.steps, l2)
 
-    # --- e2e: public API with pinned host buffers, copies in the timed region
-    hx = [x.cpu().pin_memory() for x in xs]
-    hy = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys]
-    dx = [torch.empty_like(x) for x in xs]
-    h2d = sum(x.numel() * x.element_size() for x in xs)
-    d2h = sum(y.numel() * y.element_size() for y in ys)
+    # --- e2e: public API with pinned host buffers, copies in the timed region.
+    # A step's 12 activations travel host -> device in one copy from one
+    # pinned buffer, the 12 layers run, and their outputs come back in one copy.
+    x_sizes = [x.numel() for x in xs]
+    y_sizes = [y.numel() for y in ys]
+    hx_all = torch.cat([x.reshape(-1).cpu() for x in xs]).pin_memory()
+    hy_all = torch.empty(sum(y_sizes), dtype=torch.bfloat16).pin_memory()
+    dx_all = torch.empty(hx_all.shape, dtype=torch.bfloat16, device=dev)
+    dy_all = torch.empty(hy_all.shape, dtype=torch.bfloat16, device=dev)
+    dxs, dys, o = [], [], 0
+    for (M, K, N), nx in zip(calls, x_sizes):
+        dxs.append(dx_all[o:o + nx].view(M, K))
+        o += nx
+    o = 0
+    for (M, K, N), ny in zip(calls, y_sizes):
+        dys.append(dy_all[o:o + ny].view(M, N))
+        o += ny
+    h2d = hx_all.numel() * hx_all.element_size()
+    d2h = hy_all.numel() * hy_all.element_size()
 
     def e2e_step(i):
         wset = wsets[i % nsets]
+        dx_all.copy_(hx_all, non_blocking=True)
         for j, (M, K, N) in enumerate(calls):
-            dx[j].copy_(hx[j], non_blocking=True)
             wq, sw = wset[(K, N)]
-            pkg.fp8_linear(dx[j], wq, sw, y=ys[j], workspace=wss[j], stream=stream)
-            hy[j].copy_(ys[j], non_blocking=True)
+            pkg.fp8_linear(dxs[j], wq, sw, y=dys[j], workspace=wss[j], stream=stream)
+        hy_all.copy_(dy_all, non_blocking=True)
 
     esteps = max(args.steps, 20)
     t_e2e = max_over_ranks(timed(e2e_step, esteps, 3), world)
     e2e = {"value": world * nbytes_step * esteps / t_e2e / 1e9, "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "how": "fp8_linear called from Python per layer, no graph"}
+           "how": "per step: one pinned-host H2D copy of the 12 activations, 12 fp8_linear "
+                  "calls from Python, one D2H copy of the 12 outputs"}
 
     if pkg.fp8_device_status() != pkg.FP8_OK:
         raise RuntimeError("a kernel gave up a bounded wait during the benchmark")

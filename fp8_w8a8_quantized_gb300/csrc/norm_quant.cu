@@ -31,7 +31,7 @@ namespace fp8k {
 namespace {
 
 constexpr int kBlock = 256;
-constexpr int kVPT = 4;
+constexpr int kVPT = 2;
 constexpr int64_t kLatencyChunks = 152 * 1024;
 
 template <int G, int B, bool kMax>
@@ -194,6 +194,7 @@ cudaError_t launch_rmsnorm_quant(const void* x, const void* gamma, float eps, in
     if (C <= 512 * kVPT) return launch_rows<512, kVPT>(xb, gb, eps, R, K, ldx, q, ldq, s, yb, st);
     if (C <= 1024 * kVPT)
         return launch_rows<1024, kVPT>(xb, gb, eps, R, K, ldx, q, ldq, s, yb, st);
+    if (C <= 1024 * 4) return launch_rows<1024, 4>(xb, gb, eps, R, K, ldx, q, ldq, s, yb, st);
     return cudaErrorInvalidValue;  // K > 65536: rejected by the caller
 }
 

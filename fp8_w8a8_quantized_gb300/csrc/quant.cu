@@ -17,7 +17,8 @@
 // through shared memory.  Codes leave as one 16-byte store per chunk.
 // Small problems (decode batches) use one chunk per thread, so each
 // thread's serial work -- the latency of the call -- is as short as
-// possible; large ones use four, so fewer threads carry the stream.  Very
+// possible; large ones use two (four for rows longer than 32768), the
+// measured optimum between occupancy and bytes in flight per thread.  Very
 // long rows (K > 65536) take a variant that streams the row twice.
 //
 // Memory-bound: 2 bytes in + 1 byte out per element (+4 bytes per row).
@@ -36,7 +37,7 @@ namespace fp8k {
 namespace {
 
 constexpr int kBlock = 256;  // threads per CTA for G <= 256
-constexpr int kVPT = 4;      // 16-element chunks per thread, large problems
+constexpr int kVPT = 2;      // 16-element chunks per thread, large problems (measured best)
 // Total 16-element chunks up to which the one-chunk-per-thread (latency)
 // layout is used: about one wave of 1024 threads per SM on 152 SMs.
 constexpr int64_t kLatencyChunks = 152 * 1024;
@@ -203,6 +204,7 @@ cudaError_t launch_quant_rows(const void* x, int64_t R, int64_t K, int64_t ldx, 
     if (C <= 256 * kVPT) return launch_regs<256, kVPT>(xb, R, K, ldx, q, ldq, s, st);
     if (C <= 512 * kVPT) return launch_regs<512, kVPT>(xb, R, K, ldx, q, ldq, s, st);
     if (C <= 1024 * kVPT) return launch_regs<1024, kVPT>(xb, R, K, ldx, q, ldq, s, st);
+    if (C <= 1024 * 4) return launch_regs<1024, 4>(xb, R, K, ldx, q, ldq, s, st);
     return launch_pdl(quant_rows_stream, R, 1024, st, xb, R, K, ldx, q, ldq, s);
 }
 
