@@ -27,6 +27,7 @@ struct DeviceState {
     bool ready = false;
     fp8_status_t verdict = FP8_ERR_UNSUPPORTED;
     int num_sms = 0;
+    int pair_clusters = 0;  // co-resident clusters of the paired-SM GEMM
     unsigned* status = nullptr;
 };
 
@@ -57,6 +58,7 @@ fp8_status_t current_device(DeviceState** out) {
                    fp8k::prepare_gemm_pair() != cudaSuccess) {
             d.verdict = FP8_ERR_CUDA;
         } else {
+            d.pair_clusters = fp8k::gemm_pair_resident_clusters(d.num_sms);
             d.verdict = FP8_OK;
         }
         d.ready = true;
@@ -144,6 +146,7 @@ fp8_status_t run_gemm(const uint8_t* xq, const float* s_tok, const uint8_t* wq, 
     a.num_sms = d->num_sms;
     a.pdl = true;
     a.w_early = after_quant;
+    a.pair_clusters = d->pair_clusters;
     a.stream = static_cast<cudaStream_t>(stream);
     cudaError_t e = blockwise                 ? fp8k::launch_gemm_blockwise(a)
                     : M <= fp8k::kDecodeMaxM ? fp8k::launch_gemm_decode(a)

@@ -46,6 +46,15 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float* out) {
     }
 }
 
+// k-blocks [kb0, kb0 + nkb) of split `rank` out of `splits` over nk blocks:
+// the first nk % splits splits take one block more.
+__host__ __device__ __forceinline__ void split_range(int rank, int nk, int splits, int* kb0,
+                                                     int* nkb) {
+    const int per = nk / splits, rem = nk % splits;
+    *kb0 = rank * per + (rank < rem ? rank : rem);
+    *nkb = per + (rank < rem ? 1 : 0);
+}
+
 // K-split count S (cluster size): as many clusters x splits as fill the GPU
 // with kCtasPerSm CTAs per SM in whole waves, at least 2 k-blocks per split,
 // at most kMaxSplits.

@@ -87,9 +87,8 @@ __global__ void __launch_bounds__(kThreads)
     const int n_blk = blockIdx.y;
     const uint32_t rank = cluster_ctarank();
     const int nk = (K + BK - 1) / BK;
-    const int per = nk / splits, rem = nk % splits;
-    const int kb0 = static_cast<int>(rank) * per + min(static_cast<int>(rank), rem);
-    const int nkb = per + (static_cast<int>(rank) < rem ? 1 : 0);
+    int kb0, nkb;
+    split_range(static_cast<int>(rank), nk, splits, &kb0, &nkb);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {

@@ -301,13 +301,9 @@ cudaError_t prepare_gemm_pair() {
                                 static_cast<int>(kSmemBytes));
 }
 
-// Pairs that can be resident at once (clusters of two need two free SMs of
-// one TPC); the persistent grid is sized to it.  Queried once per device.
-int co_resident_pairs(int num_sms) {
-    static int cached[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
-    if (cached[dev] > 0) return cached[dev];
+// Clusters of two that can be resident at once (a cluster needs two free SMs
+// of one TPC); the persistent grid is sized to it.
+int gemm_pair_resident_clusters(int num_sms) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     cfg.gridDim = dim3(num_sms);
@@ -322,7 +318,6 @@ int co_resident_pairs(int num_sms) {
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel, &cfg) != cudaSuccess || n <= 0)
         n = num_sms / 2;
-    cached[dev] = n;
     return n;
 }
 
@@ -331,7 +326,7 @@ cudaError_t launch_gemm_pair(const GemmArgs& a) {
     if (!encode_tmap_u8(&tmA, a.xq, a.M, a.K, a.K, BKS, BM / 2)) return cudaErrorInvalidValue;
     if (!encode_tmap_u8(&tmB, a.wq, a.N, a.K, a.K, BKS, BN / 2)) return cudaErrorInvalidValue;
     const int tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
-    const int max_pairs = co_resident_pairs(a.num_sms);
+    const int max_pairs = a.pair_clusters > 0 ? a.pair_clusters : a.num_sms / 2;
     const int pairs = tiles < max_pairs ? tiles : max_pairs;
 
     cudaLaunchConfig_t cfg = {};

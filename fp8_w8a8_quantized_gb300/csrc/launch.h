@@ -30,6 +30,7 @@ struct GemmArgs {
     // final, so the decode GEMM may load them into shared memory before its
     // griddepcontrol.wait (only the activations must wait).
     bool w_early;
+    int pair_clusters;    // co-resident clusters of the paired-SM kernel (0: unknown)
     cudaStream_t stream;
 };
 
@@ -46,6 +47,7 @@ cudaError_t launch_gemm_prefill(const GemmArgs& a);
 // M >= kPairMinM (gemm_pair.cu).
 constexpr int kPairMinM = 256;
 cudaError_t launch_gemm_pair(const GemmArgs& a);
+int gemm_pair_resident_clusters(int num_sms);
 
 // Weight-streaming split-K tcgen05 GEMM for M <= 64 (gemm_decode.cu).
 constexpr int kDecodeMaxM = 64;
