@@ -16,9 +16,15 @@
 //     flight than one deep ring (measured on GB300);
 //   * each CTA streams its K slice of W through a TMA ring; the X tile of the
 //     same K slice rides along in the same stage;
-//   * the S partial D^T tiles are summed through distributed shared memory in
-//     fixed rank order (deterministic), then scaled and stored as bf16 by
-//     all CTAs of the cluster, each owning 128/S rows.
+//   * each CTA of the cluster owns 128/S rows of the slab's output and sums
+//     their S partials in fixed rank order (deterministic), scales them and
+//     stores bf16.  Up to 16 tokens every CTA sends the partial rows of each
+//     owner straight into a dedicated receive buffer of that owner (st.async,
+//     counted on the owner's mbarrier): the partials leave as soon as the
+//     accumulator is read, and no cluster barrier is needed.  Wider token
+//     tiles (whose buffer would cost a ring stage) leave their partial in the
+//     idle ring; owners pull after a cluster barrier, and a second barrier
+//     keeps every CTA alive until its peers have read it.
 // Under programmatic dependent launch, what the kernel reads before
 // griddepcontrol.wait depends on its predecessor: after the library's own
 // quantizer (which releases it only once every earlier kernel has finished)
@@ -39,33 +45,57 @@ namespace {
 
 using namespace decode;
 constexpr int kWBoxRows = 128;  // weight tile fetched as BNW / kWBoxRows boxes
+constexpr int kMaxStages = 8;
 
 template <int MT>
 struct Cfg {
     static constexpr uint32_t X_TILE = MT * BK;
     static constexpr uint32_t STAGE_BYTES = W_TILE + X_TILE;
-    static constexpr int STAGES = (kCtaSmem - 1024 - 512) / STAGE_BYTES;
-    static_assert(STAGES >= 2, "ring depth");
-    static constexpr uint32_t RING = STAGES * STAGE_BYTES;
-    static constexpr uint32_t RED_BYTES = MT * BNW * 4;  // fp32 partial D^T, aliases the ring
-    static_assert(RED_BYTES <= RING, "partial tile must fit in the ring");
-    static_assert(STAGES <= 16, "barrier arrays hold 16 stages");
     static constexpr uint32_t TMEM_COLS = MT < 32 ? 32 : MT;
+    // Push into a dedicated receive buffer up to 16 tokens; pull beyond.
+    static constexpr bool kPush = MT <= 16;
+    static constexpr uint32_t RED_BYTES = MT * BNW * 4;  // pull: partial D^T in the ring
 };
 
 struct Bars {
-    uint64_t full[16];
-    uint64_t empty[16];
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
     uint64_t acc_full;
     uint64_t drain;
+    uint64_t recv_full;  // push: the S partials of this CTA's rows have arrived
     uint32_t tmem_base;
     int abort;
-    float s_tok[64];  // token scales, staged once for the reduction
+    float s_tok[64];   // token scales, staged for the reduction
+    float s_w[BNW];    // weight scales of the rows this CTA reduces
+};
+
+// Shared-memory layout of one launch: [ring | receive buffer | Bars], after
+// up to 1 KB of alignment.  The receive buffer (push only) holds
+// [S][rows_per][Mp + 4] fp32 partials (Mp = M rounded up to 4; the padding
+// spreads the rows of one token over the shared-memory banks).  The ring
+// gets what is left of the per-CTA budget that lets kCtasPerSm CTAs share
+// an SM.
+struct Layout {
+    uint32_t recv_bytes;
+    int stages;
+    size_t smem;
 };
 
 template <int MT>
-constexpr size_t smem_bytes() {
-    return 1024 + Cfg<MT>::RING + sizeof(Bars);
+Layout layout_of(int M, int splits) {
+    using C = Cfg<MT>;
+    Layout l;
+    const int rows_per = (BNW + splits - 1) / splits;
+    const int stride = ((M + 3) & ~3) + 4;
+    l.recv_bytes = C::kPush
+                       ? (static_cast<uint32_t>(splits * rows_per * stride * 4) + 127u) & ~127u
+                       : 0u;
+    const int64_t room =
+        static_cast<int64_t>(kCtaSmem) - 1024 - static_cast<int64_t>(sizeof(Bars)) - l.recv_bytes;
+    int st = static_cast<int>(room / C::STAGE_BYTES);
+    l.stages = st < kMaxStages ? st : kMaxStages;
+    l.smem = 1024 + static_cast<size_t>(l.stages) * C::STAGE_BYTES + l.recv_bytes + sizeof(Bars);
+    return l;
 }
 
 template <int MT>
@@ -73,14 +103,16 @@ __global__ void __launch_bounds__(kThreads)
     gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW,
                        const __grid_constant__ CUtensorMap tmX, const float* __restrict__ s_tok,
                        const float* __restrict__ s_w, __nv_bfloat16* __restrict__ y, int M, int N,
-                       int K, int splits, int w_early, unsigned* status) {
+                       int K, int splits, int stages, uint32_t recv_bytes, int w_early,
+                       unsigned* status) {
     using C = Cfg<MT>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-    Bars* bars = reinterpret_cast<Bars*>(smem + C::RING);
-    float* red = reinterpret_cast<float*>(smem);  // [MT][BNW], valid after the main loop
     uint8_t* ring = smem;
+    float* recv = reinterpret_cast<float*>(smem + stages * C::STAGE_BYTES);  // push
+    Bars* bars = reinterpret_cast<Bars*>(smem + stages * C::STAGE_BYTES + recv_bytes);
+    float* red = reinterpret_cast<float*>(smem);  // pull: [MT][BNW], after the main loop
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -89,14 +121,26 @@ __global__ void __launch_bounds__(kThreads)
     const int nk = (K + BK - 1) / BK;
     int kb0, nkb;
     split_range(static_cast<int>(rank), nk, splits, &kb0, &nkb);
+    // output rows [lo, hi) of the slab are reduced and stored by this CTA
+    const int rows_per = (BNW + splits - 1) / splits;
+    const int lo = static_cast<int>(rank) * rows_per;
+    const int hi = min(BNW, lo + rows_per);
+    const int width = hi > lo ? hi - lo : 0;
+    const int mp = (M + 3) & ~3;  // floats sent per row
+    const int stride = mp + 4;     // floats per row in the receive buffer
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::STAGES; ++s) {
+        for (int s = 0; s < stages; ++s) {
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->empty[s], 1);
         }
         mbar_init(&bars->acc_full, 1);
         mbar_init(&bars->drain, 1);
+        if constexpr (C::kPush) {
+            mbar_init(&bars->recv_full, 1);
+            mbar_arrive_expect_tx(&bars->recv_full,
+                                  static_cast<uint32_t>(splits * width * mp * 4));
+        }
         bars->abort = 0;
         fence_mbar_init();
     }
@@ -114,6 +158,10 @@ __global__ void __launch_bounds__(kThreads)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Push: peers may send partials once every CTA's barriers are
+    // initialised (first half of a split cluster barrier; the wait comes
+    // before sending).
+    if constexpr (C::kPush) cluster_arrive();
     const uint32_t tmem_base = bars->tmem_base;
     volatile int* abort_flag = &bars->abort;
 
@@ -123,25 +171,23 @@ __global__ void __launch_bounds__(kThreads)
         const uint64_t w_policy = policy_evict_first();
         // Weights before the wait: when this launch follows the library's own
         // quantizer (w_early), every earlier kernel has finished, so the first
-        // stages are filled with weights at once.  Otherwise only prefetch the
-        // first weight tiles into L2 (the point of coherence): nothing stale can
-        // reach shared memory even if the previous kernel still writes them.
-        const int pre = w_early ? (nkb < C::STAGES ? nkb : C::STAGES) : 0;
+        // stages are filled with weights at once and the next blocks are sent
+        // on their way into L2.  Otherwise only prefetch the first weight
+        // tiles into L2 (the point of coherence): nothing stale can reach
+        // shared memory even if the previous kernel still writes them.
+        const int pre = w_early ? (nkb < stages ? nkb : stages) : 0;
         if (lane == 0) {
-            if (w_early) {
-                for (int i = 0; i < pre; ++i) {
-                    mbar_arrive_expect_tx(&bars->full[i], C::STAGE_BYTES);
-                    for (int b = 0; b < BNW / kWBoxRows; ++b)
-                        tma_load_2d_hint(ring + i * C::STAGE_BYTES + b * kWBoxRows * BK, &tmW,
-                                         &bars->full[i], (kb0 + i) * BK,
-                                         n_blk * BNW + b * kWBoxRows, w_policy);
-                }
-            } else {
-                const int pf = nkb < kL2PrefetchBlocks ? nkb : kL2PrefetchBlocks;
-                for (int i = 0; i < pf; ++i)
-                    for (int b = 0; b < BNW / kWBoxRows; ++b)
-                        tma_prefetch_l2_2d(&tmW, (kb0 + i) * BK, n_blk * BNW + b * kWBoxRows);
+            for (int i = 0; i < pre; ++i) {
+                mbar_arrive_expect_tx(&bars->full[i], C::STAGE_BYTES);
+                for (int b = 0; b < BNW / kWBoxRows; ++b)
+                    tma_load_2d_hint(ring + i * C::STAGE_BYTES + b * kWBoxRows * BK, &tmW,
+                                     &bars->full[i], (kb0 + i) * BK, n_blk * BNW + b * kWBoxRows,
+                                     w_policy);
             }
+            const int pf = nkb < pre + kL2PrefetchBlocks ? nkb : pre + kL2PrefetchBlocks;
+            for (int i = pre; i < pf; ++i)
+                for (int b = 0; b < BNW / kWBoxRows; ++b)
+                    tma_prefetch_l2_2d(&tmW, (kb0 + i) * BK, n_blk * BNW + b * kWBoxRows);
         }
         __syncwarp();
         pdl_wait_primary();
@@ -150,7 +196,8 @@ __global__ void __launch_bounds__(kThreads)
                 tma_load_2d(ring + i * C::STAGE_BYTES + W_TILE, &tmX, &bars->full[i],
                             (kb0 + i) * BK, 0);
         __syncwarp();
-        uint32_t stage = pre % C::STAGES, phase = pre == C::STAGES ? 1u : 0u;
+        int stage = pre % stages;
+        uint32_t phase = pre == stages ? 1u : 0u;
         for (int i = pre; i < nkb; ++i) {
             if (!warp_wait(&bars->empty[stage], phase ^ 1u, abort_flag, status)) break;
             if (lane == 0) {
@@ -162,7 +209,7 @@ __global__ void __launch_bounds__(kThreads)
                 tma_load_2d(st + W_TILE, &tmX, &bars->full[stage], (kb0 + i) * BK, 0);
             }
             __syncwarp();
-            if (++stage == C::STAGES) {
+            if (++stage == stages) {
                 stage = 0;
                 phase ^= 1u;
             }
@@ -171,7 +218,8 @@ __global__ void __launch_bounds__(kThreads)
         // ---- MMA issuer ----
         pdl_wait_primary();
         constexpr uint32_t idesc = idesc_e4m3_f32(BNW, MT);
-        uint32_t stage = 0, phase = 0;
+        int stage = 0;
+        uint32_t phase = 0;
         bool ok = true;
         for (int i = 0; i < nkb; ++i) {
             if (!(ok = warp_wait(&bars->full[stage], phase, abort_flag, status))) break;
@@ -186,7 +234,7 @@ __global__ void __launch_bounds__(kThreads)
                 mma_commit(&bars->empty[stage]);
             }
             __syncwarp();
-            if (++stage == C::STAGES) {
+            if (++stage == stages) {
                 stage = 0;
                 phase ^= 1u;
             }
@@ -200,6 +248,16 @@ __global__ void __launch_bounds__(kThreads)
     } else {
         // ---- epilogue warps: TMEM lanes (= weight rows) of this warp's quarter ----
         pdl_wait_primary();
+        // Stage the scales the reduction needs while the main loop runs, so
+        // no global load sits between the accumulator and the output.
+        if (warp == 2) {
+            for (int m = lane; m < M; m += 32) bars->s_tok[m] = __ldg(s_tok + m);
+        } else if (warp == 3) {
+            for (int r = lo + lane; r < hi; r += 32) {
+                const int n = n_blk * BNW + r;
+                bars->s_w[r] = n < N ? __ldg(s_w + n) : 0.0f;
+            }
+        }
         const int quarter = warp & 3;
         const int nl = quarter * 32 + lane;
         float v[MT];
@@ -211,66 +269,128 @@ __global__ void __launch_bounds__(kThreads)
                 tmem_ld_cols<MT>(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16), v);
             }
         }
+        tc_fence_before();
         if (!have) {
 #pragma unroll
             for (int j = 0; j < MT; ++j) v[j] = 0.0f;
         }
-        // The ring is idle once the accumulator is complete (every stage was
-        // consumed by an MMA that has finished): reuse it for the partial.
+        if constexpr (C::kPush) {
+            // Row nl goes to the CTA that owns it, into its slot for this
+            // rank: owner.recv[rank][nl - owner.lo][0..Mp).  Sent even after
+            // a failed wait (as zeros) so that every owner's barrier completes.
+            const int owner = nl / rows_per;
+            const int rloc = nl - owner * rows_per;
+            const uint32_t dst = map_to_rank(
+                smem_u32(recv + (static_cast<int>(rank) * rows_per + rloc) * stride),
+                static_cast<uint32_t>(owner));
+            const uint32_t bar =
+                map_to_rank(smem_u32(&bars->recv_full), static_cast<uint32_t>(owner));
+            cluster_wait();
 #pragma unroll
-        for (int j = 0; j < MT; ++j) red[j * BNW + nl] = v[j];
-        if (warp == 2)
-            for (int m = lane; m < M; m += 32) bars->s_tok[m] = __ldg(s_tok + m);
+            for (int c = 0; c < MT / 4; ++c)
+                if (4 * c < M)
+                    st_async_v4(dst + 16u * c, v[4 * c], v[4 * c + 1], v[4 * c + 2],
+                                v[4 * c + 3], bar);
+        } else {
+            // The ring is idle once the accumulator is complete (every stage
+            // was consumed by an MMA that has finished): reuse it.
+#pragma unroll
+            for (int j = 0; j < MT; ++j) red[j * BNW + nl] = v[j];
+        }
     }
 
-    // All partials of the cluster are in shared memory after this barrier.
-    cluster_sync_all();
-
-    {
-        // This CTA owns weight rows [lo, hi) of the slab.  Each thread keeps
-        // one row (its weight scale in a register, its peers' partial
-        // addresses mapped once) and walks tokens m = g, g + groups, ...; the
-        // S partial loads of an output are independent, issued together and
-        // summed in rank order (deterministic).
-        const int rows_per = (BNW + splits - 1) / splits;
-        const int lo = static_cast<int>(rank) * rows_per;
-        const int hi = min(BNW, lo + rows_per);
-        const int width = hi - lo;
-        const int groups = width > 0 ? kThreads / width : 0;
-        if (groups > 0 && static_cast<int>(threadIdx.x) < groups * width) {
-            const int r = lo + static_cast<int>(threadIdx.x) % width;
-            const int n = n_blk * BNW + r;
-            const float sw = n < N ? __ldg(s_w + n) : 0.0f;
-            const uint32_t base = smem_u32(red) + static_cast<uint32_t>(r * 4);
-            uint32_t peer[kMaxSplits];
-#pragma unroll
-            for (int j = 0; j < kMaxSplits; ++j) peer[j] = j < splits ? map_to_rank(base, j) : 0u;
-#pragma unroll 4
-            for (int m = static_cast<int>(threadIdx.x) / width; m < M; m += groups) {
-                const uint32_t off = static_cast<uint32_t>(m * BNW * 4);
+    if constexpr (C::kPush) {
+        if (warp < 2) cluster_wait();
+        // every tcgen05 operation of this CTA has completed: free TMEM
+        __syncthreads();
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(tmem_base, C::TMEM_COLS);
+        }
+        // The S partials of rows [lo, hi) arrive from every CTA of the
+        // cluster (this one included).  Item i = (token i / width, row
+        // lo + i % width): a warp stores consecutive outputs of one token.
+        // Partials are summed in rank order.  Nothing remote touches this CTA
+        // afterwards, so it may exit without a barrier.
+        const bool ok =
+            warp_wait_cluster_noabort(&bars->recv_full, 0, 4 * kWaitLimitNs, status);
+        if (ok && width > 0) {
+            // walk i = threadIdx.x, +kThreads, ... as (m, r) without dividing
+            const int dm = kThreads / width, dr = kThreads - dm * width;
+            int m = static_cast<int>(threadIdx.x) / width;
+            int r = static_cast<int>(threadIdx.x) - m * width;
+            const int split_step = rows_per * stride;
+            while (m < M) {
+                const float* p = recv + r * stride + m;
                 float part[kMaxSplits];
 #pragma unroll
                 for (int j = 0; j < kMaxSplits; ++j)
-                    part[j] = j < splits ? ld_dsmem_f32(peer[j] + off) : 0.0f;
+                    part[j] = j < splits ? p[j * split_step] : 0.0f;
                 float acc = 0.0f;
 #pragma unroll
                 for (int j = 0; j < kMaxSplits; ++j)
                     if (j < splits) acc += part[j];
+                const int n = n_blk * BNW + lo + r;
                 if (n < N)
                     y[static_cast<int64_t>(m) * N + n] =
-                        __float2bfloat16_rn((acc * bars->s_tok[m]) * sw);
+                        __float2bfloat16_rn((acc * bars->s_tok[m]) * bars->s_w[lo + r]);
+                r += dr;
+                m += dm;
+                if (r >= width) {
+                    r -= width;
+                    ++m;
+                }
             }
         }
-    }
-
-    // Peers may still be reading this CTA's partial.
-    cluster_sync_all();
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        __syncwarp();
-        tc_fence_after();
-        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    } else {
+        // All partials of the cluster are in shared memory after this
+        // barrier, and every tcgen05 operation of this CTA has completed.
+        cluster_sync_all();
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(tmem_base, C::TMEM_COLS);
+        }
+        // Pull: item i = (token i / width, row lo + i % width), so a warp
+        // reads consecutive rows of one token.  A thread takes up to kItems
+        // items per round and issues all their S partial loads before
+        // summing any; partials summed in rank order.
+        constexpr int kItems = 4;
+        const int items = width * M;
+        uint32_t peer[kMaxSplits];
+#pragma unroll
+        for (int j = 0; j < kMaxSplits; ++j)
+            peer[j] = j < splits ? map_to_rank(smem_u32(red), j) : 0u;
+        for (int i0 = static_cast<int>(threadIdx.x); i0 < items; i0 += kThreads * kItems) {
+            float part[kItems][kMaxSplits];
+#pragma unroll
+            for (int p = 0; p < kItems; ++p) {
+                const int i = i0 + p * kThreads;
+                const int m = i / width;
+                const int r = lo + (i - m * width);
+                const uint32_t off = static_cast<uint32_t>((m * BNW + r) * 4);
+#pragma unroll
+                for (int j = 0; j < kMaxSplits; ++j)
+                    part[p][j] = (i < items && j < splits) ? ld_dsmem_f32(peer[j] + off) : 0.0f;
+            }
+#pragma unroll
+            for (int p = 0; p < kItems; ++p) {
+                const int i = i0 + p * kThreads;
+                if (i < items) {
+                    const int m = i / width;
+                    const int r = lo + (i - m * width);
+                    const int n = n_blk * BNW + r;
+                    float acc = 0.0f;
+#pragma unroll
+                    for (int j = 0; j < kMaxSplits; ++j)
+                        if (j < splits) acc += part[p][j];
+                    if (n < N)
+                        y[static_cast<int64_t>(m) * N + n] =
+                            __float2bfloat16_rn((acc * bars->s_tok[m]) * bars->s_w[r]);
+                }
+            }
+        }
+        // Peers may still be reading this CTA's partial.
+        cluster_sync_all();
     }
 }
 
@@ -282,12 +402,15 @@ cudaError_t launch_mt(const GemmArgs& a) {
     const int n_tiles = (a.N + BNW - 1) / BNW;
     const int nk = (a.K + BK - 1) / BK;
     const int splits = choose_splits(n_tiles, nk, a.num_sms);
+    const Layout l = layout_of<MT>(a.M, splits);
+    if (l.stages < 2 || (!Cfg<MT>::kPush && Cfg<MT>::RED_BYTES > l.stages * Cfg<MT>::STAGE_BYTES))
+        return cudaErrorInvalidConfiguration;
 
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     cfg.gridDim = dim3(splits, n_tiles);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem_bytes<MT>();
+    cfg.dynamicSmemBytes = l.smem;
     cfg.stream = a.stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = splits;
@@ -298,28 +421,22 @@ cudaError_t launch_mt(const GemmArgs& a) {
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, gemm_decode_kernel<MT>, tmW, tmX, a.s_tok, a.s_w,
-                              static_cast<__nv_bfloat16*>(a.y), a.M, a.N, a.K, splits,
-                              a.w_early ? 1 : 0, a.status);
+                              static_cast<__nv_bfloat16*>(a.y), a.M, a.N, a.K, splits, l.stages,
+                              l.recv_bytes, a.w_early ? 1 : 0, a.status);
 }
 
 }  // namespace
 
 cudaError_t prepare_gemm_decode() {
-    cudaError_t e;
     for (auto* k : {gemm_decode_kernel<16>, gemm_decode_kernel<32>, gemm_decode_kernel<64>}) {
-        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 cudaSharedmemCarveoutMaxShared);
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                             cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kCtaSmem));
         if (e != cudaSuccess) return e;
     }
-    e = cudaFuncSetAttribute(gemm_decode_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem_bytes<16>()));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gemm_decode_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem_bytes<32>()));
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(gemm_decode_kernel<64>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(smem_bytes<64>()));
+    return cudaSuccess;
 }
 
 cudaError_t launch_gemm_decode(const GemmArgs& a) {

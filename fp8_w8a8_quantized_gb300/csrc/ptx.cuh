@@ -407,6 +407,40 @@ __device__ __forceinline__ void fence_acq_rel_cluster() {
     asm volatile("fence.acq_rel.cluster;" ::: "memory");
 }
 
+// Asynchronous 16-byte store into the shared memory of a CTA of the cluster
+// (`dst` from map_to_rank); its bytes are counted (complete_tx) on the
+// mbarrier at `bar`, a shared::cluster address in the same CTA as `dst`.
+__device__ __forceinline__ void st_async_v4(uint32_t dst, float a, float b, float c, float d,
+                                            uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
+        "[%5];" ::"r"(dst),
+        "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar)
+        : "memory");
+}
+
+// Bounded wait (acquire at cluster scope) that ignores the abort flag, for a
+// barrier completed by peers' st.async bytes: every peer sends its bytes even
+// when it gave up a wait, so only a lost peer makes this give up, after
+// `limit_ns`; it then sets the status word.  Warp-uniform.
+__device__ __forceinline__ bool warp_wait_cluster_noabort(uint64_t* bar, uint32_t parity,
+                                                          uint64_t limit_ns, unsigned* status) {
+    int ok = 1;
+    if ((threadIdx.x & 31u) == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t it = 0; !mbar_try_wait_cluster(bar, parity); ++it) {
+            if ((it & 63u) == 63u && globaltimer_ns() - t0 > limit_ns) {
+                atomicOr(status, kErrWaitTimeout);
+                ok = 0;
+                break;
+            }
+        }
+    }
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
