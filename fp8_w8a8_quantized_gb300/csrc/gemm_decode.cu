@@ -98,6 +98,50 @@ Layout layout_of(int M, int splits) {
     return l;
 }
 
+// Pull reduction of the rows [lo, lo + width) this CTA owns, from the S
+// partial D^T tiles [MT][BNW] at `red` in every CTA of the cluster.  Item
+// i = (token i / width, row lo + i % width), so a warp reads consecutive
+// rows of one token.  A thread takes kItems items per round and issues all
+// their S loads before summing any (about 32 loads in flight), so each round
+// costs one distributed-shared-memory round trip; partials are summed in
+// rank order (deterministic).
+template <int S>
+__device__ __forceinline__ void pull_reduce(const float* red, int lo, int width, int M, int N,
+                                            int n_blk, const Bars* bars,
+                                            __nv_bfloat16* __restrict__ y) {
+    constexpr int kItems = S == 1 ? 16 : 32 / S;
+    const int items = width * M;
+    uint32_t peer[S];
+#pragma unroll
+    for (int j = 0; j < S; ++j) peer[j] = map_to_rank(smem_u32(red), j);
+    for (int i0 = static_cast<int>(threadIdx.x); i0 < items; i0 += kThreads * kItems) {
+        float part[kItems][S];
+#pragma unroll
+        for (int p = 0; p < kItems; ++p) {
+            const int i = i0 + p * kThreads;
+            const int m = i / width;
+            const uint32_t off = static_cast<uint32_t>((m * BNW + lo + (i - m * width)) * 4);
+#pragma unroll
+            for (int j = 0; j < S; ++j) part[p][j] = i < items ? ld_dsmem_f32(peer[j] + off) : 0.0f;
+        }
+#pragma unroll
+        for (int p = 0; p < kItems; ++p) {
+            const int i = i0 + p * kThreads;
+            if (i < items) {
+                const int m = i / width;
+                const int r = lo + (i - m * width);
+                const int n = n_blk * BNW + r;
+                float acc = 0.0f;
+#pragma unroll
+                for (int j = 0; j < S; ++j) acc += part[p][j];
+                if (n < N)
+                    y[static_cast<int64_t>(m) * N + n] =
+                        __float2bfloat16_rn((acc * bars->s_tok[m]) * bars->s_w[r]);
+            }
+        }
+    }
+}
+
 template <int MT>
 __global__ void __launch_bounds__(kThreads)
     gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW,
@@ -350,44 +394,15 @@ __global__ void __launch_bounds__(kThreads)
             tc_fence_after();
             tmem_dealloc(tmem_base, C::TMEM_COLS);
         }
-        // Pull: item i = (token i / width, row lo + i % width), so a warp
-        // reads consecutive rows of one token.  A thread takes up to kItems
-        // items per round and issues all their S partial loads before
-        // summing any; partials summed in rank order.
-        constexpr int kItems = 4;
-        const int items = width * M;
-        uint32_t peer[kMaxSplits];
-#pragma unroll
-        for (int j = 0; j < kMaxSplits; ++j)
-            peer[j] = j < splits ? map_to_rank(smem_u32(red), j) : 0u;
-        for (int i0 = static_cast<int>(threadIdx.x); i0 < items; i0 += kThreads * kItems) {
-            float part[kItems][kMaxSplits];
-#pragma unroll
-            for (int p = 0; p < kItems; ++p) {
-                const int i = i0 + p * kThreads;
-                const int m = i / width;
-                const int r = lo + (i - m * width);
-                const uint32_t off = static_cast<uint32_t>((m * BNW + r) * 4);
-#pragma unroll
-                for (int j = 0; j < kMaxSplits; ++j)
-                    part[p][j] = (i < items && j < splits) ? ld_dsmem_f32(peer[j] + off) : 0.0f;
-            }
-#pragma unroll
-            for (int p = 0; p < kItems; ++p) {
-                const int i = i0 + p * kThreads;
-                if (i < items) {
-                    const int m = i / width;
-                    const int r = lo + (i - m * width);
-                    const int n = n_blk * BNW + r;
-                    float acc = 0.0f;
-#pragma unroll
-                    for (int j = 0; j < kMaxSplits; ++j)
-                        if (j < splits) acc += part[p][j];
-                    if (n < N)
-                        y[static_cast<int64_t>(m) * N + n] =
-                            __float2bfloat16_rn((acc * bars->s_tok[m]) * bars->s_w[r]);
-                }
-            }
+        switch (splits) {
+            case 1: pull_reduce<1>(red, lo, width, M, N, n_blk, bars, y); break;
+            case 2: pull_reduce<2>(red, lo, width, M, N, n_blk, bars, y); break;
+            case 3: pull_reduce<3>(red, lo, width, M, N, n_blk, bars, y); break;
+            case 4: pull_reduce<4>(red, lo, width, M, N, n_blk, bars, y); break;
+            case 5: pull_reduce<5>(red, lo, width, M, N, n_blk, bars, y); break;
+            case 6: pull_reduce<6>(red, lo, width, M, N, n_blk, bars, y); break;
+            case 7: pull_reduce<7>(red, lo, width, M, N, n_blk, bars, y); break;
+            default: pull_reduce<8>(red, lo, width, M, N, n_blk, bars, y); break;
         }
         // Peers may still be reading this CTA's partial.
         cluster_sync_all();

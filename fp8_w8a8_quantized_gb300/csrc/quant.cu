@@ -61,10 +61,12 @@ __device__ __forceinline__ float group_max(float m, float* red) {
         const int warp = threadIdx.x >> 5;
         if (lane_id() == 0) red[warp] = m;
         __syncthreads();
+        // every lane reads one warp maximum of its group; a shuffle tree over
+        // WPG lanes combines them (max is exact in any order)
         const int first = (warp / WPG) * WPG;
-        m = red[first];
+        m = red[first + (lane_id() & (WPG - 1))];
 #pragma unroll
-        for (int w = 1; w < WPG; ++w) m = fmaxf(m, red[first + w]);
+        for (int o = WPG / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
     }
     return m;
 }

@@ -90,6 +90,49 @@ def test_ragged_layers(oracle_mod, M, N, K):
     layer(oracle_mod, x, w)
 
 
+# Decode batches (M <= 32) run as one launch that quantizes the activations
+# inside the GEMM: token counts around the tile boundaries (16/17, 32), K
+# that is not a multiple of the 128-deep k-block, ragged N, and shapes from
+# one to eight K-splits.
+@pytest.mark.parametrize("M", [2, 3, 5, 15, 16, 17, 24, 31, 32])
+@pytest.mark.parametrize("N,K", [(392, 1040), (256, 4096), (1000, 2064), (6144, 144)])
+def test_decode_batch_shapes(oracle_mod, M, N, K):
+    x = workloads.gaussian_outliers(M, K, 41 + M, DEV)
+    w = workloads.weights(N, K, 41, DEV)
+    layer(oracle_mod, x, w)
+
+
+# The stress rows (log-uniform magnitudes, all-zero rows with signed zeros,
+# exact E4M3 ties, a single 1e4 outlier, sign-mixed rows near their maximum)
+# at decode batch sizes, where the per-token scales are found inside the GEMM.
+@pytest.mark.parametrize("M", [1, 8, 16, 32])
+def test_decode_stress_rows(oracle_mod, M):
+    x, kinds = workloads.stress(DEV, M=64, K=4096)
+    # round robin over the row kinds, an all-zero row first
+    by_kind = {}
+    for r, k in enumerate(kinds):
+        by_kind.setdefault(k, []).append(r)
+    names = ["zero"] + sorted(k for k in by_kind if k != "zero")
+    order = [by_kind[k][i] for i in range(64) for k in names if i < len(by_kind[k])]
+    xs = x[torch.tensor(order[:M], device=DEV)].contiguous()
+    w = workloads.weights(1024, 4096, workloads.SEED_STRESS, DEV)
+    layer(oracle_mod, xs, w)
+
+
+def test_decode_repeatable(oracle_mod):
+    """Two calls on the same inputs give the same bits (fixed reduction order)."""
+    for M in (4, 24):
+        x = workloads.gaussian_outliers(M, 4096, 5, DEV)
+        w = workloads.weights(2048, 4096, 5, DEV)
+        wq, s_w = pkg.fp8_quant_per_channel_weights(w)
+        ws = torch.empty(pkg.fp8_linear_workspace_size(M, 2048, 4096), dtype=torch.uint8,
+                         device=DEV)
+        y1 = pkg.fp8_linear(x, wq, s_w, workspace=ws)
+        y2 = pkg.fp8_linear(x, wq, s_w, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(y1, y2)
+
+
 def test_quantized_linear_module(oracle_mod):
     x = workloads.gaussian_outliers(8, 1024, 31, DEV)
     w = workloads.weights(512, 1024, 31, DEV)
