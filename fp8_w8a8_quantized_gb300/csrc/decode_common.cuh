@@ -75,5 +75,132 @@ inline int choose_splits(int n_tiles, int nk, int num_sms) {
     return best;
 }
 
+// ---------------------------------------------------------------------------
+// Split-K reduction.  Each CTA of a cluster of S owns output rows
+// [lo, lo + width) of the 128-row slab, lo = rank * rows_per with rows_per =
+// ceil(128 / S), and sums the S partials of those rows in rank order
+// (deterministic).  `out(m, r, sum)` writes the output of token m, slab row
+// r.  Outputs are visited token-major (item i = token i / width, row lo +
+// i % width), so a warp writes consecutive outputs of one token.
+// ---------------------------------------------------------------------------
+
+// Push: the partials arrive in a receive buffer of this CTA laid out
+// [S][rows_per][stride] fp32 (stride = Mp + 4, Mp = M rounded up to 4: the
+// padding spreads the rows of one token over the banks).
+__host__ __device__ __forceinline__ int push_stride(int M) { return ((M + 3) & ~3) + 4; }
+
+__host__ __device__ __forceinline__ uint32_t push_recv_bytes(int M, int splits) {
+    const int rows_per = (BNW + splits - 1) / splits;
+    return (static_cast<uint32_t>(splits * rows_per * push_stride(M) * 4) + 127u) & ~127u;
+}
+
+// Bytes the owner of rows [lo, lo + width) receives (its mbarrier's tx count).
+__device__ __forceinline__ uint32_t push_expect_bytes(int M, int splits, int width) {
+    return static_cast<uint32_t>(splits * width * ((M + 3) & ~3) * 4);
+}
+
+// Send row nl (0..127) of this CTA's partial, v[0..M), to the CTA that owns
+// it: owner.recv[rank][nl - owner.lo][0..Mp), counted on owner.recv_full.
+template <int MT>
+__device__ __forceinline__ void push_send(const float (&v)[MT], int M, int nl, uint32_t rank,
+                                          int splits, float* recv, uint64_t* recv_full) {
+    const int rows_per = (BNW + splits - 1) / splits;
+    const int owner = nl / rows_per;
+    const int rloc = nl - owner * rows_per;
+    const uint32_t dst =
+        map_to_rank(smem_u32(recv + (static_cast<int>(rank) * rows_per + rloc) * push_stride(M)),
+                    static_cast<uint32_t>(owner));
+    const uint32_t bar = map_to_rank(smem_u32(recv_full), static_cast<uint32_t>(owner));
+#pragma unroll
+    for (int c = 0; c < MT / 4; ++c)
+        if (4 * c < M)
+            st_async_v4(dst + 16u * c, v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3], bar);
+}
+
+// Sum the received partials of rows [lo, lo + width) (call after recv_full
+// completed); every thread of the CTA takes part.
+template <typename Out>
+__device__ __forceinline__ void push_reduce(const float* recv, int splits, int lo, int width,
+                                            int M, Out out) {
+    if (width <= 0) return;
+    const int rows_per = (BNW + splits - 1) / splits;
+    const int stride = push_stride(M);
+    const int split_step = rows_per * stride;
+    // walk i = threadIdx.x, +kThreads, ... as (m, r) without dividing
+    const int dm = kThreads / width, dr = kThreads - dm * width;
+    int m = static_cast<int>(threadIdx.x) / width;
+    int r = static_cast<int>(threadIdx.x) - m * width;
+    while (m < M) {
+        const float* p = recv + r * stride + m;
+        float part[kMaxSplits];
+#pragma unroll
+        for (int j = 0; j < kMaxSplits; ++j) part[j] = j < splits ? p[j * split_step] : 0.0f;
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kMaxSplits; ++j)
+            if (j < splits) acc += part[j];
+        out(m, lo + r, acc);
+        r += dr;
+        m += dm;
+        if (r >= width) {
+            r -= width;
+            ++m;
+        }
+    }
+}
+
+// Pull: every CTA left its partial D^T tile [MT][BNW] at `red`; after a
+// cluster barrier each owner reads the S partials of its rows.  A thread
+// takes kItems items per round and issues all their S loads before summing
+// any (about 32 loads in flight), so each round costs one distributed-
+// shared-memory round trip.  A second cluster barrier must keep every CTA
+// alive until its peers have read it.
+template <int S, typename Out>
+__device__ __forceinline__ void pull_reduce_s(const float* red, int lo, int width, int M,
+                                              Out out) {
+    constexpr int kItems = S == 1 ? 16 : 32 / S;
+    const int items = width * M;
+    uint32_t peer[S];
+#pragma unroll
+    for (int j = 0; j < S; ++j) peer[j] = map_to_rank(smem_u32(red), j);
+    for (int i0 = static_cast<int>(threadIdx.x); i0 < items; i0 += kThreads * kItems) {
+        float part[kItems][S];
+#pragma unroll
+        for (int p = 0; p < kItems; ++p) {
+            const int i = i0 + p * kThreads;
+            const int m = i / width;
+            const uint32_t off = static_cast<uint32_t>((m * BNW + lo + (i - m * width)) * 4);
+#pragma unroll
+            for (int j = 0; j < S; ++j) part[p][j] = i < items ? ld_dsmem_f32(peer[j] + off) : 0.0f;
+        }
+#pragma unroll
+        for (int p = 0; p < kItems; ++p) {
+            const int i = i0 + p * kThreads;
+            if (i < items) {
+                const int m = i / width;
+                float acc = 0.0f;
+#pragma unroll
+                for (int j = 0; j < S; ++j) acc += part[p][j];
+                out(m, lo + (i - m * width), acc);
+            }
+        }
+    }
+}
+
+template <typename Out>
+__device__ __forceinline__ void pull_reduce(const float* red, int splits, int lo, int width,
+                                            int M, Out out) {
+    switch (splits) {
+        case 1: pull_reduce_s<1>(red, lo, width, M, out); break;
+        case 2: pull_reduce_s<2>(red, lo, width, M, out); break;
+        case 3: pull_reduce_s<3>(red, lo, width, M, out); break;
+        case 4: pull_reduce_s<4>(red, lo, width, M, out); break;
+        case 5: pull_reduce_s<5>(red, lo, width, M, out); break;
+        case 6: pull_reduce_s<6>(red, lo, width, M, out); break;
+        case 7: pull_reduce_s<7>(red, lo, width, M, out); break;
+        default: pull_reduce_s<8>(red, lo, width, M, out); break;
+    }
+}
+
 }  // namespace decode
 }  // namespace fp8k

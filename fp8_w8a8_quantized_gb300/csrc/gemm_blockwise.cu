@@ -279,32 +279,49 @@ namespace dc {
 
 using namespace decode;
 
+constexpr int kMaxStages = 8;
+
 template <int MT>
 struct Cfg {
     static constexpr uint32_t X_TILE = MT * BK;
     static constexpr uint32_t STAGE_BYTES = W_TILE + X_TILE;
-    static constexpr int STAGES = (kCtaSmem - 1024 - 512) / STAGE_BYTES;
-    static_assert(STAGES >= 2, "ring depth");
-    static constexpr uint32_t RING = STAGES * STAGE_BYTES;
-    static constexpr uint32_t RED_BYTES = MT * BNW * 4;
-    static_assert(RED_BYTES <= RING, "partial tile must fit in the ring");
-    static_assert(STAGES <= 16, "barrier arrays hold 16 stages");
+    static constexpr uint32_t RED_BYTES = MT * BNW * 4;  // pull: scaled partial in the ring
     static constexpr uint32_t TMEM_COLS = 2 * MT < 32 ? 32 : 2 * MT;  // two k-block buffers
+    // Push the scaled partials into a dedicated receive buffer up to 16
+    // tokens; pull beyond (as in gemm_decode.cu).
+    static constexpr bool kPush = MT <= 16;
 };
 
 struct Bars {
-    uint64_t full[16];
-    uint64_t empty[16];
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
     uint64_t kfull[2];
     uint64_t kempty[2];
     uint64_t drain;
+    uint64_t recv_full;  // push: the S partials of this CTA's rows have arrived
     uint32_t tmem_base;
     int abort;
 };
 
+// [ring | receive buffer (push) | Bars] after up to 1 KB of alignment; the
+// ring gets what is left of the budget that lets kCtasPerSm CTAs share an SM.
+struct Layout {
+    uint32_t recv_bytes;
+    int stages;
+    size_t smem;
+};
+
 template <int MT>
-constexpr size_t smem_bytes() {
-    return 1024 + Cfg<MT>::RING + sizeof(Bars);
+Layout layout_of(int M, int splits) {
+    using C = Cfg<MT>;
+    Layout l;
+    l.recv_bytes = C::kPush ? push_recv_bytes(M, splits) : 0u;
+    const int64_t room = static_cast<int64_t>(kCtaSmem) - 1024 -
+                         static_cast<int64_t>(sizeof(Bars)) - l.recv_bytes;
+    const int st = static_cast<int>(room / C::STAGE_BYTES);
+    l.stages = st < kMaxStages ? st : kMaxStages;
+    l.smem = 1024 + static_cast<size_t>(l.stages) * C::STAGE_BYTES + l.recv_bytes + sizeof(Bars);
+    return l;
 }
 
 template <int MT>
@@ -312,14 +329,16 @@ __global__ void __launch_bounds__(kThreads)
     gemm_blockwise_decode(const __grid_constant__ CUtensorMap tmW,
                           const __grid_constant__ CUtensorMap tmX, const float* __restrict__ s_x,
                           const float* __restrict__ s_w, __nv_bfloat16* __restrict__ y, int M,
-                          int N, int K, int splits, int w_early, unsigned* status) {
+                          int N, int K, int splits, int stages, uint32_t recv_bytes,
+                          int w_early, unsigned* status) {
     using C = Cfg<MT>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-    Bars* bars = reinterpret_cast<Bars*>(smem + C::RING);
-    float* red = reinterpret_cast<float*>(smem);  // [MT][BNW], valid after the main loop
     uint8_t* ring = smem;
+    float* recv = reinterpret_cast<float*>(smem + stages * C::STAGE_BYTES);  // push
+    Bars* bars = reinterpret_cast<Bars*>(smem + stages * C::STAGE_BYTES + recv_bytes);
+    float* red = reinterpret_cast<float*>(smem);  // pull: [MT][BNW], after the main loop
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -329,9 +348,14 @@ __global__ void __launch_bounds__(kThreads)
     const int per = nk / splits, rem = nk % splits;
     const int kb0 = static_cast<int>(rank) * per + min(static_cast<int>(rank), rem);
     const int nkb = per + (static_cast<int>(rank) < rem ? 1 : 0);
+    // output rows [lo, hi) of the slab are reduced and stored by this CTA
+    const int rows_per = (BNW + splits - 1) / splits;
+    const int lo = static_cast<int>(rank) * rows_per;
+    const int hi = min(BNW, lo + rows_per);
+    const int width = hi > lo ? hi - lo : 0;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::STAGES; ++s) {
+        for (int s = 0; s < stages; ++s) {
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->empty[s], 1);
         }
@@ -340,6 +364,10 @@ __global__ void __launch_bounds__(kThreads)
             mbar_init(&bars->kempty[b], 4);
         }
         mbar_init(&bars->drain, 1);
+        if constexpr (C::kPush) {
+            mbar_init(&bars->recv_full, 1);
+            mbar_arrive_expect_tx(&bars->recv_full, push_expect_bytes(M, splits, width));
+        }
         bars->abort = 0;
         fence_mbar_init();
     }
@@ -355,13 +383,15 @@ __global__ void __launch_bounds__(kThreads)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Push: peers may send partials once every CTA's barriers are initialised.
+    if constexpr (C::kPush) cluster_arrive();
     const uint32_t tmem_base = bars->tmem_base;
     volatile int* abort_flag = &bars->abort;
 
     if (warp == 0) {
         // ---- TMA producer (weights before the wait as in gemm_decode.cu) ----
         const uint64_t w_policy = policy_evict_first();
-        const int pre = w_early ? (nkb < C::STAGES ? nkb : C::STAGES) : 0;
+        const int pre = w_early ? (nkb < stages ? nkb : stages) : 0;
         if (lane == 0) {
             if (w_early) {
                 for (int i = 0; i < pre; ++i) {
@@ -382,7 +412,8 @@ __global__ void __launch_bounds__(kThreads)
                 tma_load_2d(ring + i * C::STAGE_BYTES + W_TILE, &tmX, &bars->full[i],
                             (kb0 + i) * BK, 0);
         __syncwarp();
-        uint32_t stage = pre % C::STAGES, phase = pre == C::STAGES ? 1u : 0u;
+        int stage = pre % stages;
+        uint32_t phase = pre == stages ? 1u : 0u;
         for (int i = pre; i < nkb; ++i) {
             if (!warp_wait(&bars->empty[stage], phase ^ 1u, abort_flag, status)) break;
             if (lane == 0) {
@@ -393,7 +424,7 @@ __global__ void __launch_bounds__(kThreads)
                 tma_load_2d(st + W_TILE, &tmX, &bars->full[stage], (kb0 + i) * BK, 0);
             }
             __syncwarp();
-            if (++stage == C::STAGES) {
+            if (++stage == stages) {
                 stage = 0;
                 phase ^= 1u;
             }
@@ -402,7 +433,8 @@ __global__ void __launch_bounds__(kThreads)
         // ---- MMA issuer: k-block i into TMEM buffer i % 2 ----
         pdl_wait_primary();
         constexpr uint32_t idesc = idesc_e4m3_f32(BNW, MT);
-        uint32_t stage = 0, phase = 0;
+        int stage = 0;
+        uint32_t phase = 0;
         bool ok = true;
         for (int i = 0; i < nkb; ++i) {
             const uint32_t buf = i & 1, use = static_cast<uint32_t>(i) >> 1;
@@ -420,7 +452,7 @@ __global__ void __launch_bounds__(kThreads)
                 mma_commit(&bars->kfull[buf]);
             }
             __syncwarp();
-            if (++stage == C::STAGES) {
+            if (++stage == stages) {
                 stage = 0;
                 phase ^= 1u;
             }
@@ -491,52 +523,46 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
             for (int j = 0; j < MT; ++j) acc[j] = 0.0f;
         }
-        // every MMA has finished (last kfull) and every stage was consumed:
-        // the ring is idle and holds the scaled partial tile
+        if constexpr (C::kPush) {
+            // Sent even after a failed wait (as zeros) so that every owner's
+            // barrier completes.
+            cluster_wait();
+            push_send<MT>(acc, M, nl, rank, splits, recv, &bars->recv_full);
+        } else {
+            // every MMA has finished (last kfull) and every stage was
+            // consumed: the ring is idle and holds the scaled partial tile
 #pragma unroll
-        for (int j = 0; j < MT; ++j) red[j * BNW + nl] = acc[j];
-    }
-
-    cluster_sync_all();
-
-    {
-        // This CTA owns weight rows [lo, hi) of the slab; each thread one row,
-        // the S partials of an output summed in rank order (deterministic).
-        const int rows_per = (BNW + splits - 1) / splits;
-        const int lo = static_cast<int>(rank) * rows_per;
-        const int hi = min(BNW, lo + rows_per);
-        const int width = hi - lo;
-        const int groups = width > 0 ? kThreads / width : 0;
-        if (groups > 0 && static_cast<int>(threadIdx.x) < groups * width) {
-            const int r = lo + static_cast<int>(threadIdx.x) % width;
-            const int n = n_blk * BNW + r;
-            const uint32_t base = smem_u32(red) + static_cast<uint32_t>(r * 4);
-            uint32_t peer[kMaxSplits];
-#pragma unroll
-            for (int j = 0; j < kMaxSplits; ++j) peer[j] = j < splits ? map_to_rank(base, j) : 0u;
-#pragma unroll 4
-            for (int m = static_cast<int>(threadIdx.x) / width; m < M; m += groups) {
-                const uint32_t off = static_cast<uint32_t>(m * BNW * 4);
-                float part[kMaxSplits];
-#pragma unroll
-                for (int j = 0; j < kMaxSplits; ++j)
-                    part[j] = j < splits ? ld_dsmem_f32(peer[j] + off) : 0.0f;
-                float sum = 0.0f;
-#pragma unroll
-                for (int j = 0; j < kMaxSplits; ++j)
-                    if (j < splits) sum += part[j];
-                if (n < N) y[static_cast<int64_t>(m) * N + n] = __float2bfloat16_rn(sum);
-            }
+            for (int j = 0; j < MT; ++j) red[j * BNW + nl] = acc[j];
         }
     }
 
-    cluster_sync_all();
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        __syncwarp();
-        tc_fence_after();
-        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    // the partials are already scaled: y[m, n] = bf16(sum)
+    auto store = [&](int m, int r, float sum) {
+        const int n = n_blk * BNW + r;
+        if (n < N) y[static_cast<int64_t>(m) * N + n] = __float2bfloat16_rn(sum);
+    };
+    if constexpr (C::kPush) {
+        if (warp < 2) cluster_wait();
+        // every tcgen05 operation of this CTA has completed: free TMEM
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(tmem_base, C::TMEM_COLS);
+        }
+        // Nothing remote touches this CTA after its partials have arrived.
+        if (warp_wait_cluster_noabort(&bars->recv_full, 0, 4 * kWaitLimitNs, status))
+            push_reduce(recv, splits, lo, width, M, store);
+    } else {
+        tc_fence_before();
+        cluster_sync_all();
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(tmem_base, C::TMEM_COLS);
+        }
+        pull_reduce(red, splits, lo, width, M, store);
+        // Peers may still be reading this CTA's partial.
+        cluster_sync_all();
     }
 }
 
@@ -548,12 +574,15 @@ cudaError_t launch_mt(const GemmArgs& a) {
     const int n_tiles = (a.N + BNW - 1) / BNW;
     const int nk = (a.K + BK - 1) / BK;
     const int splits = choose_splits(n_tiles, nk, a.num_sms);
+    const Layout l = layout_of<MT>(a.M, splits);
+    if (l.stages < 2 || (!Cfg<MT>::kPush && Cfg<MT>::RED_BYTES > l.stages * Cfg<MT>::STAGE_BYTES))
+        return cudaErrorInvalidConfiguration;
 
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     cfg.gridDim = dim3(splits, n_tiles);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem_bytes<MT>();
+    cfg.dynamicSmemBytes = l.smem;
     cfg.stream = a.stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = splits;
@@ -564,8 +593,8 @@ cudaError_t launch_mt(const GemmArgs& a) {
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, gemm_blockwise_decode<MT>, tmW, tmX, a.s_tok, a.s_w,
-                              static_cast<__nv_bfloat16*>(a.y), a.M, a.N, a.K, splits,
-                              a.w_early ? 1 : 0, a.status);
+                              static_cast<__nv_bfloat16*>(a.y), a.M, a.N, a.K, splits, l.stages,
+                              l.recv_bytes, a.w_early ? 1 : 0, a.status);
 }
 
 }  // namespace dc
@@ -582,18 +611,11 @@ cudaError_t prepare_gemm_blockwise() {
         e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(decode::kCtaSmem));
+        if (e != cudaSuccess) return e;
     }
-    e = cudaFuncSetAttribute(dc::gemm_blockwise_decode<16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(dc::smem_bytes<16>()));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(dc::gemm_blockwise_decode<32>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(dc::smem_bytes<32>()));
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(dc::gemm_blockwise_decode<64>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(dc::smem_bytes<64>()));
+    return cudaSuccess;
 }
 
 cudaError_t launch_gemm_blockwise(const GemmArgs& a) {

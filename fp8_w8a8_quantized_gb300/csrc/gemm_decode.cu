@@ -85,61 +85,13 @@ template <int MT>
 Layout layout_of(int M, int splits) {
     using C = Cfg<MT>;
     Layout l;
-    const int rows_per = (BNW + splits - 1) / splits;
-    const int stride = ((M + 3) & ~3) + 4;
-    l.recv_bytes = C::kPush
-                       ? (static_cast<uint32_t>(splits * rows_per * stride * 4) + 127u) & ~127u
-                       : 0u;
+    l.recv_bytes = C::kPush ? push_recv_bytes(M, splits) : 0u;
     const int64_t room =
         static_cast<int64_t>(kCtaSmem) - 1024 - static_cast<int64_t>(sizeof(Bars)) - l.recv_bytes;
     int st = static_cast<int>(room / C::STAGE_BYTES);
     l.stages = st < kMaxStages ? st : kMaxStages;
     l.smem = 1024 + static_cast<size_t>(l.stages) * C::STAGE_BYTES + l.recv_bytes + sizeof(Bars);
     return l;
-}
-
-// Pull reduction of the rows [lo, lo + width) this CTA owns, from the S
-// partial D^T tiles [MT][BNW] at `red` in every CTA of the cluster.  Item
-// i = (token i / width, row lo + i % width), so a warp reads consecutive
-// rows of one token.  A thread takes kItems items per round and issues all
-// their S loads before summing any (about 32 loads in flight), so each round
-// costs one distributed-shared-memory round trip; partials are summed in
-// rank order (deterministic).
-template <int S>
-__device__ __forceinline__ void pull_reduce(const float* red, int lo, int width, int M, int N,
-                                            int n_blk, const Bars* bars,
-                                            __nv_bfloat16* __restrict__ y) {
-    constexpr int kItems = S == 1 ? 16 : 32 / S;
-    const int items = width * M;
-    uint32_t peer[S];
-#pragma unroll
-    for (int j = 0; j < S; ++j) peer[j] = map_to_rank(smem_u32(red), j);
-    for (int i0 = static_cast<int>(threadIdx.x); i0 < items; i0 += kThreads * kItems) {
-        float part[kItems][S];
-#pragma unroll
-        for (int p = 0; p < kItems; ++p) {
-            const int i = i0 + p * kThreads;
-            const int m = i / width;
-            const uint32_t off = static_cast<uint32_t>((m * BNW + lo + (i - m * width)) * 4);
-#pragma unroll
-            for (int j = 0; j < S; ++j) part[p][j] = i < items ? ld_dsmem_f32(peer[j] + off) : 0.0f;
-        }
-#pragma unroll
-        for (int p = 0; p < kItems; ++p) {
-            const int i = i0 + p * kThreads;
-            if (i < items) {
-                const int m = i / width;
-                const int r = lo + (i - m * width);
-                const int n = n_blk * BNW + r;
-                float acc = 0.0f;
-#pragma unroll
-                for (int j = 0; j < S; ++j) acc += part[p][j];
-                if (n < N)
-                    y[static_cast<int64_t>(m) * N + n] =
-                        __float2bfloat16_rn((acc * bars->s_tok[m]) * bars->s_w[r]);
-            }
-        }
-    }
 }
 
 template <int MT>
@@ -170,8 +122,6 @@ __global__ void __launch_bounds__(kThreads)
     const int lo = static_cast<int>(rank) * rows_per;
     const int hi = min(BNW, lo + rows_per);
     const int width = hi > lo ? hi - lo : 0;
-    const int mp = (M + 3) & ~3;  // floats sent per row
-    const int stride = mp + 4;     // floats per row in the receive buffer
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -182,8 +132,7 @@ __global__ void __launch_bounds__(kThreads)
         mbar_init(&bars->drain, 1);
         if constexpr (C::kPush) {
             mbar_init(&bars->recv_full, 1);
-            mbar_arrive_expect_tx(&bars->recv_full,
-                                  static_cast<uint32_t>(splits * width * mp * 4));
+            mbar_arrive_expect_tx(&bars->recv_full, push_expect_bytes(M, splits, width));
         }
         bars->abort = 0;
         fence_mbar_init();
@@ -319,22 +268,10 @@ __global__ void __launch_bounds__(kThreads)
             for (int j = 0; j < MT; ++j) v[j] = 0.0f;
         }
         if constexpr (C::kPush) {
-            // Row nl goes to the CTA that owns it, into its slot for this
-            // rank: owner.recv[rank][nl - owner.lo][0..Mp).  Sent even after
-            // a failed wait (as zeros) so that every owner's barrier completes.
-            const int owner = nl / rows_per;
-            const int rloc = nl - owner * rows_per;
-            const uint32_t dst = map_to_rank(
-                smem_u32(recv + (static_cast<int>(rank) * rows_per + rloc) * stride),
-                static_cast<uint32_t>(owner));
-            const uint32_t bar =
-                map_to_rank(smem_u32(&bars->recv_full), static_cast<uint32_t>(owner));
+            // Sent even after a failed wait (as zeros) so that every owner's
+            // barrier completes.
             cluster_wait();
-#pragma unroll
-            for (int c = 0; c < MT / 4; ++c)
-                if (4 * c < M)
-                    st_async_v4(dst + 16u * c, v[4 * c], v[4 * c + 1], v[4 * c + 2],
-                                v[4 * c + 3], bar);
+            push_send<MT>(v, M, nl, rank, splits, recv, &bars->recv_full);
         } else {
             // The ring is idle once the accumulator is complete (every stage
             // was consumed by an MMA that has finished): reuse it.
@@ -343,6 +280,13 @@ __global__ void __launch_bounds__(kThreads)
         }
     }
 
+    // y[m, n] = bf16((sum * s_tok[m]) * s_w[n]) for slab row r
+    auto store = [&](int m, int r, float acc) {
+        const int n = n_blk * BNW + r;
+        if (n < N)
+            y[static_cast<int64_t>(m) * N + n] =
+                __float2bfloat16_rn((acc * bars->s_tok[m]) * bars->s_w[r]);
+    };
     if constexpr (C::kPush) {
         if (warp < 2) cluster_wait();
         // every tcgen05 operation of this CTA has completed: free TMEM
@@ -352,40 +296,10 @@ __global__ void __launch_bounds__(kThreads)
             tmem_dealloc(tmem_base, C::TMEM_COLS);
         }
         // The S partials of rows [lo, hi) arrive from every CTA of the
-        // cluster (this one included).  Item i = (token i / width, row
-        // lo + i % width): a warp stores consecutive outputs of one token.
-        // Partials are summed in rank order.  Nothing remote touches this CTA
+        // cluster (this one included).  Nothing remote touches this CTA
         // afterwards, so it may exit without a barrier.
-        const bool ok =
-            warp_wait_cluster_noabort(&bars->recv_full, 0, 4 * kWaitLimitNs, status);
-        if (ok && width > 0) {
-            // walk i = threadIdx.x, +kThreads, ... as (m, r) without dividing
-            const int dm = kThreads / width, dr = kThreads - dm * width;
-            int m = static_cast<int>(threadIdx.x) / width;
-            int r = static_cast<int>(threadIdx.x) - m * width;
-            const int split_step = rows_per * stride;
-            while (m < M) {
-                const float* p = recv + r * stride + m;
-                float part[kMaxSplits];
-#pragma unroll
-                for (int j = 0; j < kMaxSplits; ++j)
-                    part[j] = j < splits ? p[j * split_step] : 0.0f;
-                float acc = 0.0f;
-#pragma unroll
-                for (int j = 0; j < kMaxSplits; ++j)
-                    if (j < splits) acc += part[j];
-                const int n = n_blk * BNW + lo + r;
-                if (n < N)
-                    y[static_cast<int64_t>(m) * N + n] =
-                        __float2bfloat16_rn((acc * bars->s_tok[m]) * bars->s_w[lo + r]);
-                r += dr;
-                m += dm;
-                if (r >= width) {
-                    r -= width;
-                    ++m;
-                }
-            }
-        }
+        if (warp_wait_cluster_noabort(&bars->recv_full, 0, 4 * kWaitLimitNs, status))
+            push_reduce(recv, splits, lo, width, M, store);
     } else {
         // All partials of the cluster are in shared memory after this
         // barrier, and every tcgen05 operation of this CTA has completed.
@@ -394,16 +308,7 @@ __global__ void __launch_bounds__(kThreads)
             tc_fence_after();
             tmem_dealloc(tmem_base, C::TMEM_COLS);
         }
-        switch (splits) {
-            case 1: pull_reduce<1>(red, lo, width, M, N, n_blk, bars, y); break;
-            case 2: pull_reduce<2>(red, lo, width, M, N, n_blk, bars, y); break;
-            case 3: pull_reduce<3>(red, lo, width, M, N, n_blk, bars, y); break;
-            case 4: pull_reduce<4>(red, lo, width, M, N, n_blk, bars, y); break;
-            case 5: pull_reduce<5>(red, lo, width, M, N, n_blk, bars, y); break;
-            case 6: pull_reduce<6>(red, lo, width, M, N, n_blk, bars, y); break;
-            case 7: pull_reduce<7>(red, lo, width, M, N, n_blk, bars, y); break;
-            default: pull_reduce<8>(red, lo, width, M, N, n_blk, bars, y); break;
-        }
+        pull_reduce(red, splits, lo, width, M, store);
         // Peers may still be reading this CTA's partial.
         cluster_sync_all();
     }
