@@ -131,6 +131,7 @@ __global__ void __launch_bounds__(G > kBlock ? G : kBlock)
     }
     m = group_reduce<G, B, true>(m, red);
     const float sc = scale_of(m);
+    const Divisor dv = divisor_of(sc);
     if (!live) return;
     uint4* qr = reinterpret_cast<uint4*>(q + row * ldq);
     uint4* yr = y_out ? reinterpret_cast<uint4*>(y_out + row * K) : nullptr;
@@ -138,8 +139,8 @@ __global__ void __launch_bounds__(G > kBlock ? G : kBlock)
     for (int i = 0; i < VPT; ++i) {
         const int64_t c = t + static_cast<int64_t>(i) * G;
         if (c < C) {
-            const uint2 a = quant8(v[i][0], sc);
-            const uint2 b = quant8(v[i][1], sc);
+            const uint2 a = quant8(v[i][0], dv);
+            const uint2 b = quant8(v[i][1], dv);
             qr[c] = make_uint4(a.x, a.y, b.x, b.y);
             if (yr) {
                 yr[2 * c] = v[i][0];

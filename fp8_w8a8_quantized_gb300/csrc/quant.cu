@@ -22,8 +22,10 @@
 // long rows (K > 65536) take a variant that streams the row twice.
 //
 // Memory-bound: 2 bytes in + 1 byte out per element (+4 bytes per row).
-// Divisions use __fdiv_rn (IEEE round-to-nearest); nothing here is compiled
-// with fast-math or flush-to-zero, so results are bit-identical to the fp32
+// The scale is an IEEE division; each quotient x / s is the correctly rounded
+// fp32 value, from one reciprocal per row and a multiply and two fused
+// multiply-adds per element (quant_math.cuh).  Nothing here is compiled with
+// fast-math or flush-to-zero, so results are bit-identical to the fp32
 // definition above.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -105,13 +107,14 @@ __global__ void __launch_bounds__(G > kBlock ? G : kBlock)
     m = group_max<G, B>(m, red);
     const float sc = scale_of(m);
     if (!live) return;
+    const Divisor dv = divisor_of(sc);
     uint4* qr = reinterpret_cast<uint4*>(q + row * ldq);
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         const int64_t c = t + static_cast<int64_t>(i) * G;
         if (c < C) {
-            const uint2 a = quant8(v[i][0], sc);
-            const uint2 b = quant8(v[i][1], sc);
+            const uint2 a = quant8(v[i][0], dv);
+            const uint2 b = quant8(v[i][1], dv);
             qr[c] = make_uint4(a.x, a.y, b.x, b.y);
         }
     }
@@ -136,10 +139,11 @@ __global__ void __launch_bounds__(1024)
     }
     m = group_max<1024, 1024>(m, red);
     const float sc = scale_of(m);
+    const Divisor dv = divisor_of(sc);
     uint4* qr = reinterpret_cast<uint4*>(q + row * ldq);
     for (int64_t c = threadIdx.x; c < C; c += 1024) {
-        const uint2 a = quant8(ld_stream(xr + 2 * c), sc);
-        const uint2 b = quant8(ld_stream(xr + 2 * c + 1), sc);
+        const uint2 a = quant8(ld_stream(xr + 2 * c), dv);
+        const uint2 b = quant8(ld_stream(xr + 2 * c + 1), dv);
         qr[c] = make_uint4(a.x, a.y, b.x, b.y);
     }
     if (threadIdx.x == 0) s[row] = sc;

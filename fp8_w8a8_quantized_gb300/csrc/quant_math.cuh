@@ -2,7 +2,7 @@
 // and the quantizers with other scale granularities (quant_variants.cu), so
 // all produce the same bytes:
 //   amax = max |x| (exact in fp32), s = amax / 448 (IEEE fp32 division) or 1,
-//   q = E4M3_rn_satfinite(x / s) (IEEE fp32 quotient).
+//   q = E4M3_rn_satfinite(x / s) (the correctly rounded fp32 quotient).
 // "FP8 Inference Explained, in depth", "Scales and their granularity";
 // "Quantization: FP8 inference and KV-cache quantization", "Dynamic scales or
 // static scales".
@@ -32,20 +32,61 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
     return r;
 }
 
+// x / s rounded to nearest fp32, for a scale s > 0 shared by many x,
+// without a division per element.  Markstein's division theorem (P.
+// Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Develop. 34(1), 1990; also "IA-64 and
+// Elementary Functions", 2000): with r = RN(1/s) and a quotient q0 within
+// one ulp of x/s (here q0 = RN(x * r)), the residual e = x - s * q0 is exact
+// in one fused multiply-add and RN(q0 + e * r) = RN(x / s) whenever the
+// quotient is a normal number.  Quotients below the normal range can only
+// become an E4M3 zero, where an ulp does not matter; the sign of zero is
+// that of x (s > 0), as for the IEEE quotient.  A quotient that overflows
+// (a small static scale) stays infinite and saturates like the IEEE one.  A
+// scale whose reciprocal is not a normal number (s below the normal range or
+// above 2^126), or that is not finite, takes the IEEE division.
+struct Divisor {
+    float s, r;
+    bool ieee;
+};
+
+__device__ __forceinline__ Divisor divisor_of(float s) {
+    Divisor d;
+    d.s = s;
+    d.r = __frcp_rn(s);
+    d.ieee = !(s >= 1.17549435e-38f && s <= 8.50705917e37f);  // [2^-126, 2^126]
+    return d;
+}
+
+// RN(x / s) for a scale on the fast path (d.ieee false).
+__device__ __forceinline__ float div_rn(float x, const Divisor& d) {
+    const float q0 = __fmul_rn(x, d.r);
+    const float e = __fmaf_rn(-q0, d.s, x);
+    const float q = copysignf(__fmaf_rn(e, d.r, q0), x);
+    return isinf(q0) ? q0 : q;
+}
+
 // One bf16 pair -> two codes in the low 16 bits.
-__device__ __forceinline__ uint32_t quant2(uint32_t u, float s) {
+__device__ __forceinline__ uint32_t quant2(uint32_t u, const Divisor& d) {
+    return cvt_e4m3x2(div_rn(bf16lo(u), d), div_rn(bf16hi(u), d));
+}
+
+__device__ __forceinline__ uint32_t quant2_ieee(uint32_t u, float s) {
     return cvt_e4m3x2(__fdiv_rn(bf16lo(u), s), __fdiv_rn(bf16hi(u), s));
 }
 
-// Four bf16 values (8 bytes) -> four codes packed in one 32-bit word.
-__device__ __forceinline__ uint32_t quant4(const uint2& v, float s) {
-    return quant2(v.x, s) | (quant2(v.y, s) << 16);
+// Scales outside the fast path's range: out of line, so that the common
+// path keeps its registers.
+static __device__ __noinline__ uint2 quant8_ieee(uint4 v, float s) {
+    return make_uint2(quant2_ieee(v.x, s) | (quant2_ieee(v.y, s) << 16),
+                      quant2_ieee(v.z, s) | (quant2_ieee(v.w, s) << 16));
 }
 
 // Eight bf16 values (16 bytes) -> eight codes packed in two 32-bit words.
-__device__ __forceinline__ uint2 quant8(const uint4& v, float s) {
-    return make_uint2(quant2(v.x, s) | (quant2(v.y, s) << 16),
-                      quant2(v.z, s) | (quant2(v.w, s) << 16));
+__device__ __forceinline__ uint2 quant8(const uint4& v, const Divisor& d) {
+    if (d.ieee) return quant8_ieee(v, d.s);
+    return make_uint2(quant2(v.x, d) | (quant2(v.y, d) << 16),
+                      quant2(v.z, d) | (quant2(v.w, d) << 16));
 }
 
 __device__ __forceinline__ float scale_of(float amax) {

@@ -27,9 +27,9 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int64_t kGroup = 128;  // block edge of the block-wise scales
 
-__device__ __forceinline__ uint4 quant16(const uint4* src, float s) {
+__device__ __forceinline__ uint4 quant16(const uint4* src, const Divisor& d) {
     const uint4 a = __ldg(src), b = __ldg(src + 1);
-    const uint2 qa = quant8(a, s), qb = quant8(b, s);
+    const uint2 qa = quant8(a, d), qb = quant8(b, d);
     return make_uint4(qa.x, qa.y, qb.x, qb.y);
 }
 
@@ -40,11 +40,12 @@ __device__ __forceinline__ void quant_chunks(const uint16_t* __restrict__ x, int
                                              int64_t ldq) {
     const int64_t C = K >> 4;
     const int64_t total = R * C;
+    const Divisor dv = divisor_of(s);
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * kThreads) {
         const int64_t r = i / C, c = i - r * C;
         const uint4* src = reinterpret_cast<const uint4*>(x + r * ldx + c * 16);
-        *reinterpret_cast<uint4*>(q + r * ldq + c * 16) = quant16(src, s);
+        *reinterpret_cast<uint4*>(q + r * ldq + c * 16) = quant16(src, dv);
     }
 }
 
@@ -135,7 +136,8 @@ __global__ void __launch_bounds__(kThreads)
         if (row < 0 || row >= n_slots) continue;
         const float s = __ldg(scale + h * scale_stride);
         const uint4* src = reinterpret_cast<const uint4*>(x + th * D + c * 16);
-        *reinterpret_cast<uint4*>(cache + (row * H + h) * D + c * 16) = quant16(src, s);
+        *reinterpret_cast<uint4*>(cache + (row * H + h) * D + c * 16) =
+            quant16(src, divisor_of(s));
     }
 }
 
@@ -169,7 +171,8 @@ __global__ void __launch_bounds__(kThreads)
         for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
         const float sc = scale_of(m);
         if (live) {
-            const uint2 qa = quant8(a, sc), qb = quant8(b, sc);
+            const Divisor dv = divisor_of(sc);
+            const uint2 qa = quant8(a, dv), qb = quant8(b, dv);
             *reinterpret_cast<uint4*>(q + r * ldq + k) = make_uint4(qa.x, qa.y, qb.x, qb.y);
             if (sub == 0) s[r * KB + kb] = sc;
         }
@@ -201,11 +204,12 @@ __global__ void __launch_bounds__(kThreads)
         m = amax8(v[i][1], amax8(v[i][0], m));
     }
     const float sc = scale_of(block_max(m, red));
+    const Divisor dv = divisor_of(sc);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int64_t n = nb * kGroup + (threadIdx.x >> 3) + 32 * i;
         if (n < N && k < K) {
-            const uint2 qa = quant8(v[i][0], sc), qb = quant8(v[i][1], sc);
+            const uint2 qa = quant8(v[i][0], dv), qb = quant8(v[i][1], dv);
             *reinterpret_cast<uint4*>(q + n * ldq + k) = make_uint4(qa.x, qa.y, qb.x, qb.y);
         }
     }
