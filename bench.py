@@ -372,6 +372,7 @@ def run_ours(args):
                "workload": "llama-3.1-8b prefill layers, M in {2048,8192}, 8 fp8_linear calls"}
     del pxs, pys, pws
 
+    decode_70b = decode_70b_rates(pkg, workloads, dev, stream, timed, hbm_peak, args.steps, l2)
     variants = variant_rates(pkg, workloads, dev, stream, timed, hbm_peak, args.steps)
     blockwise = blockwise_rates(pkg, workloads, dev, stream, timed, hbm_peak, fp8_peak,
                                 args.steps, l2)
@@ -438,6 +439,7 @@ def run_ours(args):
             "roofline": roofline,
             "prefill": prefill,
             "scale_variants": variants,
+            "decode_70b": decode_70b,
             "blockwise": blockwise,
             "e2e": e2e,
             "cpu_baseline": cpu,
@@ -525,6 +527,59 @@ def blockwise_rates(pkg, workloads, dev, stream, timed, hbm_peak, fp8_peak, step
     torch.cuda.empty_cache()
     return {"decode": decode, "prefill": prefill,
             "launches_per_decode_step": 2 * len(calls)}
+
+
+def decode_70b_rates(pkg, workloads, dev, stream, timed, hbm_peak, steps, l2):
+    """The 70B-shaped decode layers (32 tokens; QKV, O, gate/up, down: 68 to
+    470 MB of E4M3 weights each), one step = 4 fp8_linear calls in a CUDA
+    graph, weights rotated over two sets (1.7 GB > 2 x L2)."""
+    import torch
+
+    calls = [(32, K, N) for (_, K, N) in workloads.SHAPES_70B]
+    per_set = sum(N * K for (_, K, N) in workloads.SHAPES_70B)
+    nsets = max(2, -(-2 * l2 // per_set) + 1)
+    wsets = []
+    for s_ in range(nsets):
+        d = {}
+        for (_, K, N) in workloads.SHAPES_70B:
+            w = workloads.weights(N, K, workloads.SEED_70B + 100 * s_, dev)
+            d[(K, N)] = pkg.fp8_quant_per_channel_weights(w)
+            del w
+        wsets.append(d)
+    xs = [workloads.gaussian_outliers(M, K, workloads.SEED_70B, dev) for (M, K, N) in calls]
+    ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for (M, K, N) in calls]
+    wss = [torch.empty(pkg.fp8_linear_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+           for (M, K, N) in calls]
+    torch.cuda.synchronize()
+
+    def step(wset, st):
+        for i, (M, K, N) in enumerate(calls):
+            wq, sw = wset[(K, N)]
+            pkg.fp8_linear(xs[i], wq, sw, y=ys[i], workspace=wss[i], stream=st)
+
+    graphs = []
+    with torch.cuda.stream(stream):
+        for wset in wsets:
+            step(wset, stream)
+        stream.synchronize()
+        for wset in wsets:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(wset, torch.cuda.current_stream())
+            graphs.append(g)
+    torch.cuda.synchronize()
+    n = max(steps, 50)
+    t = timed(lambda i: graphs[i % nsets].replay(), n, 3)
+    nbytes = sum(layer_bytes(M, K, N) for (M, K, N) in calls)
+    gbs = nbytes * n / t / 1e9
+    del graphs, xs, ys, wss, wsets
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return {"gbs": gbs, "frac": gbs / hbm_peak, "ms_per_step": t / n * 1e3,
+            "bytes_per_step": nbytes,
+            "workload": "llama-3.1-70b decode linear layers at 32 tokens: (K,N) in "
+                        "{(8192,10240),(8192,8192),(8192,57344),(28672,8192)}, 4 fp8_linear "
+                        "calls per step"}
 
 
 def variant_rates(pkg, workloads, dev, stream, timed, hbm_peak, steps):

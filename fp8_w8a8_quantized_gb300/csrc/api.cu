@@ -28,6 +28,7 @@ struct DeviceState {
     fp8_status_t verdict = FP8_ERR_UNSUPPORTED;
     int num_sms = 0;
     int pair_clusters = 0;  // co-resident clusters of the paired-SM GEMM
+    int decode_clusters[9] = {};  // co-resident clusters of S decode-GEMM CTAs, S = 1..8
     unsigned* status = nullptr;
 };
 
@@ -59,6 +60,8 @@ fp8_status_t current_device(DeviceState** out) {
             d.verdict = FP8_ERR_CUDA;
         } else {
             d.pair_clusters = fp8k::gemm_pair_resident_clusters(d.num_sms);
+            for (int c = 1; c <= 8; ++c)
+                d.decode_clusters[c] = fp8k::gemm_decode_resident_clusters(c);
             d.verdict = FP8_OK;
         }
         d.ready = true;
@@ -147,6 +150,7 @@ fp8_status_t run_gemm(const uint8_t* xq, const float* s_tok, const uint8_t* wq, 
     a.pdl = true;
     a.w_early = after_quant;
     a.pair_clusters = d->pair_clusters;
+    a.decode_clusters = d->decode_clusters;
     a.stream = static_cast<cudaStream_t>(stream);
     cudaError_t e = blockwise                 ? fp8k::launch_gemm_blockwise(a)
                     : M <= fp8k::kDecodeMaxM ? fp8k::launch_gemm_decode(a)

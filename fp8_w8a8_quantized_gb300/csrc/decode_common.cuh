@@ -55,18 +55,23 @@ __host__ __device__ __forceinline__ void split_range(int rank, int nk, int split
     *nkb = per + (rank < rem ? 1 : 0);
 }
 
-// K-split count S (cluster size): as many clusters x splits as fill the GPU
-// with kCtasPerSm CTAs per SM in whole waves, at least 2 k-blocks per split,
-// at most kMaxSplits.
-inline int choose_splits(int n_tiles, int nk, int num_sms) {
+// K-split count S (cluster size): the one whose grid (n_tiles clusters of S
+// CTAs) keeps the largest share of the kCtasPerSm x num_sms CTA slots busy
+// over its waves, with at least 2 k-blocks per split and S <= kMaxSplits.
+// A cluster must fit on the SMs of one GPC, so fewer than slots / S clusters
+// of S may be resident at once: clusters[S], when known, is that number and
+// sets the waves (measured on GB300: 64 clusters of 7 do not fit, 74 of 6
+// do).
+inline int choose_splits(int n_tiles, int nk, int num_sms, const int* clusters = nullptr) {
     const int slots = kCtasPerSm * num_sms;
     int best = 1;
     double best_eff = -1.0;
     for (int s = 1; s <= kMaxSplits; ++s) {
         if (s > 1 && nk < 2 * s) break;
-        const int ctas = n_tiles * s;
-        const int waves = (ctas + slots - 1) / slots;
-        const double eff = static_cast<double>(ctas) / (static_cast<double>(waves) * slots);
+        const int per_wave = (clusters && clusters[s] > 0) ? clusters[s] : slots / s;
+        if (per_wave < 1) break;
+        const int waves = (n_tiles + per_wave - 1) / per_wave;
+        const double eff = static_cast<double>(n_tiles) * s / (static_cast<double>(waves) * slots);
         if (eff > best_eff + 0.02) {
             best_eff = eff;
             best = s;

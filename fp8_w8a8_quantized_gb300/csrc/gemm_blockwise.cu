@@ -573,7 +573,7 @@ cudaError_t launch_mt(const GemmArgs& a) {
     if (!encode_tmap_u8(&tmX, a.xq, a.M, a.K, a.K, BK, MT)) return cudaErrorInvalidValue;
     const int n_tiles = (a.N + BNW - 1) / BNW;
     const int nk = (a.K + BK - 1) / BK;
-    const int splits = choose_splits(n_tiles, nk, a.num_sms);
+    const int splits = choose_splits(n_tiles, nk, a.num_sms, a.decode_clusters);
     const Layout l = layout_of<MT>(a.M, splits);
     if (l.stages < 2 || (!Cfg<MT>::kPush && Cfg<MT>::RED_BYTES > l.stages * Cfg<MT>::STAGE_BYTES))
         return cudaErrorInvalidConfiguration;

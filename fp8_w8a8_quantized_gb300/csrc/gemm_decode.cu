@@ -321,7 +321,7 @@ cudaError_t launch_mt(const GemmArgs& a) {
     if (!encode_tmap_u8(&tmX, a.xq, a.M, a.K, a.K, BK, MT)) return cudaErrorInvalidValue;
     const int n_tiles = (a.N + BNW - 1) / BNW;
     const int nk = (a.K + BK - 1) / BK;
-    const int splits = choose_splits(n_tiles, nk, a.num_sms);
+    const int splits = choose_splits(n_tiles, nk, a.num_sms, a.decode_clusters);
     const Layout l = layout_of<MT>(a.M, splits);
     if (l.stages < 2 || (!Cfg<MT>::kPush && Cfg<MT>::RED_BYTES > l.stages * Cfg<MT>::STAGE_BYTES))
         return cudaErrorInvalidConfiguration;
@@ -345,7 +345,42 @@ cudaError_t launch_mt(const GemmArgs& a) {
                               l.recv_bytes, a.w_early ? 1 : 0, a.status);
 }
 
+// Never launched: the occupancy calculator's stand-in for the decode GEMMs
+// (same block size and shared-memory footprint, which is what limits them
+// to kCtasPerSm CTAs per SM).  Asked about the real kernels, the calculator
+// reports one CTA per SM for cluster launches, while three are resident
+// (measured); for this stand-in it reports the residency that is measured.
+__global__ void __launch_bounds__(kThreads) decode_residency_probe() {}
+
 }  // namespace
+
+int gemm_decode_resident_clusters(int size) {
+    if (cudaFuncSetAttribute(decode_residency_probe, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kCtaSmem)) != cudaSuccess ||
+        cudaFuncSetAttribute(decode_residency_probe,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(size, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kCtaSmem;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = size;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, decode_residency_probe, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
 
 cudaError_t prepare_gemm_decode() {
     for (auto* k : {gemm_decode_kernel<16>, gemm_decode_kernel<32>, gemm_decode_kernel<64>}) {

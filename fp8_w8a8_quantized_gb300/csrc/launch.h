@@ -31,6 +31,9 @@ struct GemmArgs {
     // griddepcontrol.wait (only the activations must wait).
     bool w_early;
     int pair_clusters;    // co-resident clusters of the paired-SM kernel (0: unknown)
+    // decode_clusters[S]: clusters of S decode-GEMM CTAs that can be resident
+    // at once (index 1..8; null or 0: unknown)
+    const int* decode_clusters = nullptr;
     cudaStream_t stream;
 };
 
@@ -52,6 +55,9 @@ int gemm_pair_resident_clusters(int num_sms);
 // Weight-streaming split-K tcgen05 GEMM for M <= 64 (gemm_decode.cu).
 constexpr int kDecodeMaxM = 64;
 cudaError_t launch_gemm_decode(const GemmArgs& a);
+// How many clusters of `size` decode-GEMM CTAs can be resident at once (a
+// cluster must fit on the SMs of one GPC); 0 if unknown.
+int gemm_decode_resident_clusters(int size);
 
 // Quantization with other scale granularities (quant_variants.cu).
 // Every row quantized with the scale *s; s_rows (optional) gets s per row.
