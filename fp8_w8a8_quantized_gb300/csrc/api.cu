@@ -134,8 +134,8 @@ fp8_status_t check_gemm(const uint8_t* xq, const float* s_tok, const uint8_t* wq
 }
 
 fp8_status_t run_gemm(const uint8_t* xq, const float* s_tok, const uint8_t* wq, const float* s_w,
-                      void* y, int64_t M, int64_t N, int64_t K, bool after_quant, void* stream,
-                      DeviceState* d, bool blockwise = false) {
+                      void* y, int64_t M, int64_t N, int64_t K, void* stream, DeviceState* d,
+                      bool blockwise = false) {
     fp8k::GemmArgs a;
     a.xq = xq;
     a.s_tok = s_tok;
@@ -148,7 +148,6 @@ fp8_status_t run_gemm(const uint8_t* xq, const float* s_tok, const uint8_t* wq, 
     a.status = d->status;
     a.num_sms = d->num_sms;
     a.pdl = true;
-    a.w_early = after_quant;
     a.pair_clusters = d->pair_clusters;
     a.decode_clusters = d->decode_clusters;
     a.stream = static_cast<cudaStream_t>(stream);
@@ -208,7 +207,7 @@ fp8_status_t fp8_scaled_gemm(const uint8_t* xq, const float* s_tok, const uint8_
     // be anything (even the kernel writing wq): before its griddepcontrol.wait
     // the GEMM only prefetches weights into L2, the point of coherence, so an
     // early start cannot read stale inputs.
-    return run_gemm(xq, s_tok, wq, s_w, y_bf16, M, N, K, false, stream, d);
+    return run_gemm(xq, s_tok, wq, s_w, y_bf16, M, N, K, stream, d);
 }
 
 size_t fp8_linear_workspace_size(int64_t M, int64_t N, int64_t K) {
@@ -245,12 +244,13 @@ fp8_status_t fp8_linear(const void* x_bf16, const uint8_t* wq, const float* s_w,
     cudaError_t e = fp8k::launch_quant_rows(x_bf16, M, K, K, xq, K, s_tok,
                                             static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return FP8_ERR_CUDA;
-    // Both launches are programmatic dependents of their predecessor.  The
-    // quantizer waits before touching memory and releases the GEMM only after
-    // that wait, so every earlier kernel (any writer of wq) has finished when
-    // the GEMM starts: it may stream weights before its own wait, and reads
-    // the quantized activations after it.
-    return run_gemm(xq, s_tok, wq, s_w, y_bf16, M, N, K, true, stream, d);
+    // Both launches are programmatic dependents of their predecessor and
+    // release their own dependents at their start.  Before its
+    // griddepcontrol.wait the GEMM only prefetches weights into L2; the wait
+    // returns once the quantizer has completed, and the quantizer completes
+    // only after its own wait (every earlier kernel, any writer of wq or x,
+    // has finished).
+    return run_gemm(xq, s_tok, wq, s_w, y_bf16, M, N, K, stream, d);
 }
 
 fp8_status_t fp8_quant_static(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,
@@ -344,7 +344,7 @@ fp8_status_t fp8_scaled_gemm_blockwise(const uint8_t* xq, const float* s_x, cons
     if (st != FP8_OK || M == 0 || N == 0) return st;
     DeviceState* d = nullptr;
     if ((st = current_device(&d)) != FP8_OK) return st;
-    return run_gemm(xq, s_x, wq, s_w, y_bf16, M, N, K, false, stream, d, true);
+    return run_gemm(xq, s_x, wq, s_w, y_bf16, M, N, K, stream, d, true);
 }
 
 size_t fp8_linear_blockwise_workspace_size(int64_t M, int64_t N, int64_t K) {
@@ -374,9 +374,9 @@ fp8_status_t fp8_linear_blockwise(const void* x_bf16, const uint8_t* wq, const f
     cudaError_t e = fp8k::launch_quant_groups(x_bf16, M, K, K, xq, K, s_x, d->num_sms,
                                               static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return FP8_ERR_CUDA;
-    // as in fp8_linear: the quantizer releases the GEMM only after its own
-    // wait, so the GEMM may stream weights before its griddepcontrol.wait
-    return run_gemm(xq, s_x, wq, s_w, y_bf16, M, N, K, true, stream, d, true);
+    // as in fp8_linear: the GEMM reads nothing but L2 prefetches before its
+    // griddepcontrol.wait, which returns once the quantizer has completed
+    return run_gemm(xq, s_x, wq, s_w, y_bf16, M, N, K, stream, d, true);
 }
 
 fp8_status_t fp8_rmsnorm_quant(const void* x_bf16, const void* gamma_bf16, float eps, int64_t M,
@@ -417,9 +417,10 @@ fp8_status_t fp8_linear_rmsnorm(const void* x_bf16, const void* gamma_bf16, floa
     cudaError_t e = fp8k::launch_rmsnorm_quant(x_bf16, gamma_bf16, eps, M, K, K, xq, K, s_tok,
                                                nullptr, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return FP8_ERR_CUDA;
-    // as in fp8_linear: the producer of the codes releases the GEMM only after
-    // its own wait, so the GEMM may stream weights before its wait
-    return run_gemm(xq, s_tok, wq, s_w, y_bf16, M, N, K, true, stream, d);
+    // as in fp8_linear: the GEMM reads nothing but L2 prefetches before its
+    // griddepcontrol.wait, which returns once the producer of the codes has
+    // completed
+    return run_gemm(xq, s_tok, wq, s_w, y_bf16, M, N, K, stream, d);
 }
 
 const char* fp8_status_string(fp8_status_t status) {

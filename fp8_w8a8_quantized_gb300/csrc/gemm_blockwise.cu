@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(kThreads)
                           const __grid_constant__ CUtensorMap tmX, const float* __restrict__ s_x,
                           const float* __restrict__ s_w, __nv_bfloat16* __restrict__ y, int M,
                           int N, int K, int splits, int stages, uint32_t recv_bytes,
-                          int w_early, unsigned* status) {
+                          unsigned* status) {
     using C = Cfg<MT>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -389,32 +389,18 @@ __global__ void __launch_bounds__(kThreads)
     volatile int* abort_flag = &bars->abort;
 
     if (warp == 0) {
-        // ---- TMA producer (weights before the wait as in gemm_decode.cu) ----
+        // ---- TMA producer (only L2 prefetches before the wait, as in
+        // gemm_decode.cu) ----
         const uint64_t w_policy = policy_evict_first();
-        const int pre = w_early ? (nkb < stages ? nkb : stages) : 0;
         if (lane == 0) {
-            if (w_early) {
-                for (int i = 0; i < pre; ++i) {
-                    mbar_arrive_expect_tx(&bars->full[i], C::STAGE_BYTES);
-                    tma_load_2d_hint(ring + i * C::STAGE_BYTES, &tmW, &bars->full[i],
-                                     (kb0 + i) * BK, n_blk * BNW, w_policy);
-                }
-            } else {
-                const int pf = nkb < kL2PrefetchBlocks ? nkb : kL2PrefetchBlocks;
-                for (int i = 0; i < pf; ++i)
-                    tma_prefetch_l2_2d(&tmW, (kb0 + i) * BK, n_blk * BNW);
-            }
+            const int pf = nkb < kL2PrefetchBlocks ? nkb : kL2PrefetchBlocks;
+            for (int i = 0; i < pf; ++i) tma_prefetch_l2_2d(&tmW, (kb0 + i) * BK, n_blk * BNW);
         }
         __syncwarp();
         pdl_wait_primary();
-        if (lane == 0)
-            for (int i = 0; i < pre; ++i)
-                tma_load_2d(ring + i * C::STAGE_BYTES + W_TILE, &tmX, &bars->full[i],
-                            (kb0 + i) * BK, 0);
-        __syncwarp();
-        int stage = pre % stages;
-        uint32_t phase = pre == stages ? 1u : 0u;
-        for (int i = pre; i < nkb; ++i) {
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int i = 0; i < nkb; ++i) {
             if (!warp_wait(&bars->empty[stage], phase ^ 1u, abort_flag, status)) break;
             if (lane == 0) {
                 uint8_t* st = ring + stage * C::STAGE_BYTES;
@@ -594,7 +580,7 @@ cudaError_t launch_mt(const GemmArgs& a) {
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, gemm_blockwise_decode<MT>, tmW, tmX, a.s_tok, a.s_w,
                               static_cast<__nv_bfloat16*>(a.y), a.M, a.N, a.K, splits, l.stages,
-                              l.recv_bytes, a.w_early ? 1 : 0, a.status);
+                              l.recv_bytes, a.status);
 }
 
 }  // namespace dc

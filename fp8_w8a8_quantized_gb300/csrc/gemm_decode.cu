@@ -25,11 +25,10 @@
 //     tiles (whose buffer would cost a ring stage) leave their partial in the
 //     idle ring; owners pull after a cluster barrier, and a second barrier
 //     keeps every CTA alive until its peers have read it.
-// Under programmatic dependent launch, what the kernel reads before
-// griddepcontrol.wait depends on its predecessor: after the library's own
-// quantizer (which releases it only once every earlier kernel has finished)
-// it fills its ring with weights at once; otherwise it only prefetches the
-// first weight tiles into L2, so an early start cannot observe stale inputs.
+// Under programmatic dependent launch the kernel may start while earlier
+// kernels still run (the quantizer before it releases it at once): before
+// griddepcontrol.wait it only prefetches its first weight tiles into L2, the
+// point of coherence, so an early start cannot observe stale inputs.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -99,8 +98,7 @@ __global__ void __launch_bounds__(kThreads)
     gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW,
                        const __grid_constant__ CUtensorMap tmX, const float* __restrict__ s_tok,
                        const float* __restrict__ s_w, __nv_bfloat16* __restrict__ y, int M, int N,
-                       int K, int splits, int stages, uint32_t recv_bytes, int w_early,
-                       unsigned* status) {
+                       int K, int splits, int stages, uint32_t recv_bytes, unsigned* status) {
     using C = Cfg<MT>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -162,36 +160,20 @@ __global__ void __launch_bounds__(kThreads)
     if (warp == 0) {
         // ---- TMA producer ----
         const uint64_t w_policy = policy_evict_first();
-        // Weights before the wait: when this launch follows the library's own
-        // quantizer (w_early), every earlier kernel has finished, so the first
-        // stages are filled with weights at once and the next blocks are sent
-        // on their way into L2.  Otherwise only prefetch the first weight
-        // tiles into L2 (the point of coherence): nothing stale can reach
-        // shared memory even if the previous kernel still writes them.
-        const int pre = w_early ? (nkb < stages ? nkb : stages) : 0;
+        // Before the wait only prefetch the first weight tiles into L2 (the
+        // point of coherence): nothing stale can reach shared memory even if
+        // an earlier kernel still writes them.
         if (lane == 0) {
-            for (int i = 0; i < pre; ++i) {
-                mbar_arrive_expect_tx(&bars->full[i], C::STAGE_BYTES);
-                for (int b = 0; b < BNW / kWBoxRows; ++b)
-                    tma_load_2d_hint(ring + i * C::STAGE_BYTES + b * kWBoxRows * BK, &tmW,
-                                     &bars->full[i], (kb0 + i) * BK, n_blk * BNW + b * kWBoxRows,
-                                     w_policy);
-            }
-            const int pf = nkb < pre + kL2PrefetchBlocks ? nkb : pre + kL2PrefetchBlocks;
-            for (int i = pre; i < pf; ++i)
+            const int pf = nkb < kL2PrefetchBlocks ? nkb : kL2PrefetchBlocks;
+            for (int i = 0; i < pf; ++i)
                 for (int b = 0; b < BNW / kWBoxRows; ++b)
                     tma_prefetch_l2_2d(&tmW, (kb0 + i) * BK, n_blk * BNW + b * kWBoxRows);
         }
         __syncwarp();
         pdl_wait_primary();
-        if (lane == 0)
-            for (int i = 0; i < pre; ++i)
-                tma_load_2d(ring + i * C::STAGE_BYTES + W_TILE, &tmX, &bars->full[i],
-                            (kb0 + i) * BK, 0);
-        __syncwarp();
-        int stage = pre % stages;
-        uint32_t phase = pre == stages ? 1u : 0u;
-        for (int i = pre; i < nkb; ++i) {
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int i = 0; i < nkb; ++i) {
             if (!warp_wait(&bars->empty[stage], phase ^ 1u, abort_flag, status)) break;
             if (lane == 0) {
                 uint8_t* st = ring + stage * C::STAGE_BYTES;
@@ -342,7 +324,7 @@ cudaError_t launch_mt(const GemmArgs& a) {
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, gemm_decode_kernel<MT>, tmW, tmX, a.s_tok, a.s_w,
                               static_cast<__nv_bfloat16*>(a.y), a.M, a.N, a.K, splits, l.stages,
-                              l.recv_bytes, a.w_early ? 1 : 0, a.status);
+                              l.recv_bytes, a.status);
 }
 
 // Never launched: the occupancy calculator's stand-in for the decode GEMMs

@@ -25,11 +25,6 @@ struct GemmArgs {
     unsigned* status;     // device status word
     int num_sms;
     bool pdl;             // launch as a programmatic dependent of the previous kernel
-    // The previous kernel is this library's quantizer, which releases its
-    // dependents only after every earlier kernel has finished: the weights are
-    // final, so the decode GEMM may load them into shared memory before its
-    // griddepcontrol.wait (only the activations must wait).
-    bool w_early;
     int pair_clusters;    // co-resident clusters of the paired-SM kernel (0: unknown)
     // decode_clusters[S]: clusters of S decode-GEMM CTAs that can be resident
     // at once (index 1..8; null or 0: unknown)

@@ -95,8 +95,8 @@ __global__ void __launch_bounds__(G > kBlock ? G : kBlock)
     constexpr int B = G > kBlock ? G : kBlock;
     constexpr int ROWS = B / G;
     __shared__ float red[B / 32];
-    pdl_wait_primary();
     pdl_launch_dependents();
+    pdl_wait_primary();
 
     const int64_t row = static_cast<int64_t>(blockIdx.x) * ROWS + threadIdx.x / G;
     const int t = threadIdx.x % G;

@@ -80,12 +80,12 @@ __global__ void __launch_bounds__(G > kBlock ? G : kBlock)
     constexpr int B = G > kBlock ? G : kBlock;
     constexpr int ROWS = B / G;
     __shared__ float red[B / 32];
-    // Launched as a programmatic dependent: wait for the previous kernel
-    // before touching memory, and only then let the next kernel start -- so
-    // when a dependent GEMM starts, every kernel before this one has finished
-    // (it may then read the weights before its own wait).
-    pdl_wait_primary();
+    // Launched as a programmatic dependent: the next kernel may start at
+    // once (it reads nothing but L2 prefetches before its own wait, which
+    // returns after this grid has completed); this one waits for its
+    // predecessor before touching memory.
     pdl_launch_dependents();
+    pdl_wait_primary();
 
     const int64_t row = static_cast<int64_t>(blockIdx.x) * ROWS + threadIdx.x / G;
     const int t = threadIdx.x % G;
@@ -127,8 +127,8 @@ __global__ void __launch_bounds__(1024)
     quant_rows_stream(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx,
                       uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s) {
     __shared__ float red[32];
-    pdl_wait_primary();
     pdl_launch_dependents();
+    pdl_wait_primary();
     const int64_t row = blockIdx.x;
     const int64_t C = K >> 4;
     const uint4* xr = reinterpret_cast<const uint4*>(x + row * ldx);
@@ -151,8 +151,8 @@ __global__ void __launch_bounds__(1024)
 
 // K == 0: an empty row has amax 0, so its scale is 1.
 __global__ void fill_ones(float* s, int64_t R) {
-    pdl_wait_primary();
     pdl_launch_dependents();
+    pdl_wait_primary();
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i < R) s[i] = 1.0f;
 }
@@ -160,7 +160,8 @@ __global__ void fill_ones(float* s, int64_t R) {
 // Every kernel here waits (griddepcontrol.wait) before reading or writing
 // global memory, so it is always launched as a programmatic dependent of the
 // previous kernel on the stream: its launch overlaps that kernel's tail.  It
-// releases its own dependents only after that wait.
+// releases its own dependents at its start: they too touch nothing but L2
+// before their own wait, which returns once this grid has completed.
 template <typename... Params, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(Params...), int64_t grid, int block, cudaStream_t st,
                        Args... args) {

@@ -61,8 +61,8 @@ __global__ void __launch_bounds__(kThreads)
     quant_given_scale(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx,
                       const float* __restrict__ s_ptr, uint8_t* __restrict__ q, int64_t ldq,
                       float* __restrict__ s_rows) {
-    pdl_wait_primary();
     pdl_launch_dependents();
+    pdl_wait_primary();
     const float s = __ldg(s_ptr);
     quant_chunks(x, R, K, ldx, s, q, ldq);
     if (s_rows) fill_rows(s_rows, R, s);
@@ -85,8 +85,8 @@ __global__ void __launch_bounds__(kThreads)
     tensor_amax_partial(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx,
                         float* __restrict__ partial) {
     __shared__ float red[kThreads / 32];
-    pdl_wait_primary();
     pdl_launch_dependents();
+    pdl_wait_primary();
     const int64_t C = K >> 4;
     const int64_t total = R * C;
     float m = 0.0f;
@@ -107,8 +107,8 @@ __global__ void __launch_bounds__(kThreads)
                  const float* __restrict__ partial, int n_partial, uint8_t* __restrict__ q,
                  int64_t ldq, float* __restrict__ s_out, float* __restrict__ s_rows) {
     __shared__ float red[kThreads / 32];
-    pdl_wait_primary();
     pdl_launch_dependents();
+    pdl_wait_primary();
     float m = 0.0f;
     for (int i = threadIdx.x; i < n_partial; i += kThreads) m = fmaxf(m, partial[i]);
     const float s = scale_of(block_max(m, red));
@@ -124,8 +124,8 @@ __global__ void __launch_bounds__(kThreads)
                    const float* __restrict__ scale, int64_t scale_stride,
                    const int64_t* __restrict__ slot, uint8_t* __restrict__ cache,
                    int64_t n_slots) {
-    pdl_wait_primary();
     pdl_launch_dependents();
+    pdl_wait_primary();
     const int64_t C = D >> 4;  // chunks per head
     const int64_t total = T * H * C;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < total;
@@ -148,8 +148,8 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(kThreads)
     quant_groups(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx,
                  uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s, int64_t KB) {
-    pdl_wait_primary();
     pdl_launch_dependents();
+    pdl_wait_primary();
     const int lane = lane_id();
     const int sub = lane & 7;
     const int64_t groups = R * KB;
@@ -186,8 +186,8 @@ __global__ void __launch_bounds__(kThreads)
     quant_weight_blocks(const uint16_t* __restrict__ w, int64_t N, int64_t K, int64_t ldw,
                         uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s) {
     __shared__ float red[kThreads / 32];
-    pdl_wait_primary();
     pdl_launch_dependents();
+    pdl_wait_primary();
     const int64_t kb = blockIdx.x, nb = blockIdx.y, KB = gridDim.x;
     const int64_t k = kb * kGroup + (threadIdx.x & 7) * 16;
     uint4 v[4][2];
