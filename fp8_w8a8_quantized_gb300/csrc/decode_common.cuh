@@ -24,7 +24,7 @@ constexpr int kCtasPerSm = 3;
 constexpr uint32_t kSmemPerSm = 228 * 1024;
 constexpr uint32_t kCtaSmem = kSmemPerSm / kCtasPerSm - 1024;  // 1 KB reserved per CTA
 constexpr uint32_t kCtaSmem2 = kSmemPerSm / 2 - 1024;           // two CTAs per SM
-constexpr int kL2PrefetchBlocks = 8;  // k-blocks of W prefetched into L2 before the wait
+constexpr int kL2PrefetchBlocks = 4;  // k-blocks of W prefetched into L2 before the wait (measured)
 
 // Accumulator columns of one warp's 32 TMEM lanes -> registers.
 template <int MT>

@@ -312,12 +312,12 @@ struct Layout {
 };
 
 template <int MT>
-Layout layout_of(int M, int splits) {
+Layout layout_of(int M, int splits, int64_t budget) {
     using C = Cfg<MT>;
     Layout l;
     l.recv_bytes = C::kPush ? push_recv_bytes(M, splits) : 0u;
-    const int64_t room = static_cast<int64_t>(kCtaSmem) - 1024 -
-                         static_cast<int64_t>(sizeof(Bars)) - l.recv_bytes;
+    const int64_t room =
+        budget - 1024 - static_cast<int64_t>(sizeof(Bars)) - l.recv_bytes;
     const int st = static_cast<int>(room / C::STAGE_BYTES);
     l.stages = st < kMaxStages ? st : kMaxStages;
     l.smem = 1024 + static_cast<size_t>(l.stages) * C::STAGE_BYTES + l.recv_bytes + sizeof(Bars);
@@ -560,7 +560,10 @@ cudaError_t launch_mt(const GemmArgs& a) {
     const int n_tiles = (a.N + BNW - 1) / BNW;
     const int nk = (a.K + BK - 1) / BK;
     const int splits = choose_splits(n_tiles, nk, a.num_sms, a.decode_clusters);
-    const Layout l = layout_of<MT>(a.M, splits);
+    // as in gemm_decode.cu: a grid of at most two CTAs per SM gets the
+    // two-per-SM budget (deeper ring)
+    const bool two = static_cast<int64_t>(n_tiles) * splits <= 2 * a.num_sms;
+    const Layout l = layout_of<MT>(a.M, splits, two ? kCtaSmem2 : kCtaSmem);
     if (l.stages < 2 || (!Cfg<MT>::kPush && Cfg<MT>::RED_BYTES > l.stages * Cfg<MT>::STAGE_BYTES))
         return cudaErrorInvalidConfiguration;
 
@@ -598,7 +601,7 @@ cudaError_t prepare_gemm_blockwise() {
                                  cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(decode::kCtaSmem));
+                                 static_cast<int>(decode::kCtaSmem2));
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
