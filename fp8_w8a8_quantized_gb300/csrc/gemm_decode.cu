@@ -51,8 +51,6 @@ struct Cfg {
     static constexpr uint32_t X_TILE = MT * BK;
     static constexpr uint32_t STAGE_BYTES = W_TILE + X_TILE;
     static constexpr uint32_t TMEM_COLS = MT < 32 ? 32 : MT;
-    // Push into a dedicated receive buffer up to 16 tokens; pull beyond.
-    static constexpr bool kPush = MT <= 16;
     static constexpr uint32_t RED_BYTES = MT * BNW * 4;  // pull: partial D^T in the ring
 };
 
@@ -80,11 +78,11 @@ struct Layout {
     size_t smem;
 };
 
-template <int MT>
+template <int MT, bool PUSH>
 Layout layout_of(int M, int splits, int64_t budget) {
     using C = Cfg<MT>;
     Layout l;
-    l.recv_bytes = C::kPush ? push_recv_bytes(M, splits) : 0u;
+    l.recv_bytes = PUSH ? push_recv_bytes(M, splits) : 0u;
     const int64_t room =
         budget - 1024 - static_cast<int64_t>(sizeof(Bars)) - l.recv_bytes;
     int st = static_cast<int>(room / C::STAGE_BYTES);
@@ -93,7 +91,9 @@ Layout layout_of(int M, int splits, int64_t budget) {
     return l;
 }
 
-template <int MT>
+// PUSH: partials pushed into a dedicated receive buffer (no cluster barrier
+// after the main loop); otherwise pulled from the idle ring.
+template <int MT, bool PUSH>
 __global__ void __launch_bounds__(kThreads)
     gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW,
                        const __grid_constant__ CUtensorMap tmX, const float* __restrict__ s_tok,
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kThreads)
         }
         mbar_init(&bars->acc_full, 1);
         mbar_init(&bars->drain, 1);
-        if constexpr (C::kPush) {
+        if constexpr (PUSH) {
             mbar_init(&bars->recv_full, 1);
             mbar_arrive_expect_tx(&bars->recv_full, push_expect_bytes(M, splits, width));
         }
@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(kThreads)
     // Push: peers may send partials once every CTA's barriers are
     // initialised (first half of a split cluster barrier; the wait comes
     // before sending).
-    if constexpr (C::kPush) cluster_arrive();
+    if constexpr (PUSH) cluster_arrive();
     const uint32_t tmem_base = bars->tmem_base;
     volatile int* abort_flag = &bars->abort;
 
@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
             for (int j = 0; j < MT; ++j) v[j] = 0.0f;
         }
-        if constexpr (C::kPush) {
+        if constexpr (PUSH) {
             // Sent even after a failed wait (as zeros) so that every owner's
             // barrier completes.
             cluster_wait();
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kThreads)
             y[static_cast<int64_t>(m) * N + n] =
                 __float2bfloat16_rn((acc * bars->s_tok[m]) * bars->s_w[r]);
     };
-    if constexpr (C::kPush) {
+    if constexpr (PUSH) {
         if (warp < 2) cluster_wait();
         // every tcgen05 operation of this CTA has completed: free TMEM
         __syncthreads();
@@ -296,20 +296,14 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-template <int MT>
-cudaError_t launch_mt(const GemmArgs& a) {
+template <int MT, bool PUSH>
+cudaError_t launch_mt(const GemmArgs& a, int splits, bool two) {
     CUtensorMap tmW, tmX;
     if (!encode_tmap_u8(&tmW, a.wq, a.N, a.K, a.K, BK, kWBoxRows)) return cudaErrorInvalidValue;
     if (!encode_tmap_u8(&tmX, a.xq, a.M, a.K, a.K, BK, MT)) return cudaErrorInvalidValue;
     const int n_tiles = (a.N + BNW - 1) / BNW;
-    const int nk = (a.K + BK - 1) / BK;
-    const int splits = choose_splits(n_tiles, nk, a.num_sms, a.decode_clusters);
-    // A grid of at most two CTAs per SM gets the two-per-SM budget: a 4-5
-    // stage ring instead of 3 (measured on the 8B decode step, 3852 -> 3923
-    // GB/s; limiting it to token tiles of up to 16 was slower).
-    const bool two = static_cast<int64_t>(n_tiles) * splits <= 2 * a.num_sms;
-    const Layout l = layout_of<MT>(a.M, splits, two ? kCtaSmem2 : kCtaSmem);
-    if (l.stages < 2 || (!Cfg<MT>::kPush && Cfg<MT>::RED_BYTES > l.stages * Cfg<MT>::STAGE_BYTES))
+    const Layout l = layout_of<MT, PUSH>(a.M, splits, two ? kCtaSmem2 : kCtaSmem);
+    if (l.stages < 2 || (!PUSH && Cfg<MT>::RED_BYTES > l.stages * Cfg<MT>::STAGE_BYTES))
         return cudaErrorInvalidConfiguration;
 
     cudaLaunchConfig_t cfg = {};
@@ -326,7 +320,7 @@ cudaError_t launch_mt(const GemmArgs& a) {
     attr[1].val.programmaticStreamSerializationAllowed = a.pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, gemm_decode_kernel<MT>, tmW, tmX, a.s_tok, a.s_w,
+    return cudaLaunchKernelEx(&cfg, gemm_decode_kernel<MT, PUSH>, tmW, tmX, a.s_tok, a.s_w,
                               static_cast<__nv_bfloat16*>(a.y), a.M, a.N, a.K, splits, l.stages,
                               l.recv_bytes, a.status);
 }
@@ -369,7 +363,8 @@ int gemm_decode_resident_clusters(int size) {
 }
 
 cudaError_t prepare_gemm_decode() {
-    for (auto* k : {gemm_decode_kernel<16>, gemm_decode_kernel<32>, gemm_decode_kernel<64>}) {
+    for (auto* k :
+         {gemm_decode_kernel<16, true>, gemm_decode_kernel<32, false>, gemm_decode_kernel<64, false>}) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                              cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
@@ -381,9 +376,18 @@ cudaError_t prepare_gemm_decode() {
 }
 
 cudaError_t launch_gemm_decode(const GemmArgs& a) {
-    if (a.M <= 16) return launch_mt<16>(a);
-    if (a.M <= 32) return launch_mt<32>(a);
-    return launch_mt<64>(a);
+    const int n_tiles = (a.N + BNW - 1) / BNW;
+    const int splits = choose_splits(n_tiles, (a.K + BK - 1) / BK, a.num_sms, a.decode_clusters);
+    // A grid of at most two CTAs per SM gets the two-per-SM budget: a 4-5
+    // stage ring instead of 3 (measured on the 8B decode step, 3852 -> 3923
+    // GB/s; limiting it to token tiles of up to 16 was slower).  Partials are
+    // pushed up to 16 tokens and pulled beyond (pushing at 32 tokens in the
+    // two-per-SM grids, where the receive buffer fits beside a 4-stage ring,
+    // measured 3924 against 3960 GB/s for the step).
+    const bool two = static_cast<int64_t>(n_tiles) * splits <= 2 * a.num_sms;
+    if (a.M <= 16) return launch_mt<16, true>(a, splits, two);
+    if (a.M <= 32) return launch_mt<32, false>(a, splits, two);
+    return launch_mt<64, false>(a, splits, two);
 }
 
 }  // namespace fp8k
