@@ -373,6 +373,7 @@ def run_ours(args):
     del pxs, pys, pws
 
     decode_70b = decode_70b_rates(pkg, workloads, dev, stream, timed, hbm_peak, args.steps, l2)
+    prefill_70b = prefill_70b_rate(pkg, workloads, dev, stream, timed, fp8_peak, args.steps)
     variants = variant_rates(pkg, workloads, dev, stream, timed, hbm_peak, args.steps)
     blockwise = blockwise_rates(pkg, workloads, dev, stream, timed, hbm_peak, fp8_peak,
                                 args.steps, l2)
@@ -485,6 +486,7 @@ def run_ours(args):
             "prefill": prefill,
             "scale_variants": variants,
             "decode_70b": decode_70b,
+            "prefill_70b": prefill_70b,
             "blockwise": blockwise,
             "e2e": e2e,
             "cpu_baseline": cpu,
@@ -572,6 +574,42 @@ def blockwise_rates(pkg, workloads, dev, stream, timed, hbm_peak, fp8_peak, step
     torch.cuda.empty_cache()
     return {"decode": decode, "prefill": prefill,
             "launches_per_decode_step": 2 * len(calls)}
+
+
+def prefill_70b_rate(pkg, workloads, dev, stream, timed, fp8_peak, steps):
+    """The 70B-shaped layers at 4096 tokens (config 4's prefill batch): one
+    step = 4 fp8_linear calls (QKV, O, gate/up, down), TFLOPS."""
+    import torch
+
+    calls = [(4096, K, N) for (_, K, N) in workloads.SHAPES_70B]
+    ws_ = {}
+    for (_, K, N) in workloads.SHAPES_70B:
+        w = workloads.weights(N, K, workloads.SEED_70B, dev)
+        ws_[(K, N)] = pkg.fp8_quant_per_channel_weights(w)
+        del w
+    xs = {}
+    for (M, K, N) in calls:
+        if (M, K) not in xs:
+            xs[(M, K)] = workloads.gaussian_outliers(M, K, workloads.SEED_70B, dev)
+    ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for (M, K, N) in calls]
+    wsp = torch.empty(max(pkg.fp8_linear_workspace_size(M, N, K) for (M, K, N) in calls),
+                      dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    def step(i):
+        for j, (M, K, N) in enumerate(calls):
+            wq, sw = ws_[(K, N)]
+            pkg.fp8_linear(xs[(M, K)], wq, sw, y=ys[j], workspace=wsp, stream=stream)
+
+    n = max(3, min(steps, 10))
+    t = timed(step, n, 2)
+    tflops = sum(2 * M * N * K for (M, K, N) in calls) * n / t / 1e12
+    del xs, ys, wsp, ws_
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return {"tflops": tflops, "frac": tflops / fp8_peak, "frac_of_4500_nominal": tflops / 4500.0,
+            "workload": "llama-3.1-70b layers at 4096 tokens: (K,N) in {(8192,10240),(8192,8192),"
+                        "(8192,57344),(28672,8192)}, 4 fp8_linear calls per step"}
 
 
 def decode_70b_rates(pkg, workloads, dev, stream, timed, hbm_peak, steps, l2):
