@@ -29,6 +29,14 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Every call is asynchronous on that stream and never
  *     synchronizes the host.
+ *   - Kernels are launched with programmatic stream serialization: one may
+ *     start while the previous work on the stream drains, but reads no
+ *     global memory except L2 prefetches of weights before all of that work
+ *     has completed, so stream order holds for the caller's data.  Each
+ *     kernel also lets its successor on the stream launch early; a caller's
+ *     kernel launched with programmatic stream serialization after one of
+ *     these calls must execute griddepcontrol.wait (cudaGridDependencySynchronize)
+ *     before reading the call's outputs, as any such kernel must.
  *   - Layouts are row-major.  Activations X are [M, K] (tokens x in-features),
  *     weights W are [N, K] (out-features x in-features, the nn.Linear layout,
  *     K contiguous), outputs Y are [M, N] bf16 with leading dimension N.
