@@ -234,8 +234,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_32x32b_x16(taddr + h * 16, r);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        acc[h * 16 + j] = fmaf(__uint_as_float(r[j]), c, acc[h * 16 + j]);
+                    for (int j = 0; j < 16; j += 2)
+                        fma2(acc[h * 16 + j], acc[h * 16 + j + 1], __uint_as_float(r[j]),
+                             __uint_as_float(r[j + 1]), c, c);
                 }
                 tc_fence_before();
                 __syncwarp();

@@ -316,6 +316,20 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// (a0, a1) = (b0 * c0 + a0, b1 * c1 + a1): two fp32 fused multiply-adds
+// (round to nearest, as fmaf) in one packed f32x2 instruction.
+__device__ __forceinline__ void fma2(float& a0, float& a1, float b0, float b1, float c0,
+                                     float c1) {
+    asm("{\n\t.reg .b64 pa, pb, pc;\n\t"
+        "mov.b64 pa, {%0, %1};\n\t"
+        "mov.b64 pb, {%2, %3};\n\t"
+        "mov.b64 pc, {%4, %5};\n\t"
+        "fma.rn.f32x2 pa, pb, pc, pa;\n\t"
+        "mov.b64 {%0, %1}, pa;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA, tcgen05.mma operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
