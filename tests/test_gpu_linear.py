@@ -90,15 +90,23 @@ def test_ragged_layers(oracle_mod, M, N, K):
     layer(oracle_mod, x, w)
 
 
-# Decode batches (M <= 32) run as one launch that quantizes the activations
-# inside the GEMM: token counts around the tile boundaries (16/17, 32), K
-# that is not a multiple of the 128-deep k-block, ragged N, and shapes from
-# one to eight K-splits.
-@pytest.mark.parametrize("M", [2, 3, 5, 15, 16, 17, 24, 31, 32])
+# Decode batches (M <= 32): one token, token counts around the tile
+# boundaries (16/17, 32), K that is not a multiple of the 128-deep k-block,
+# ragged N, and shapes from one to eight K-splits.
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 15, 16, 17, 24, 31, 32])
 @pytest.mark.parametrize("N,K", [(392, 1040), (256, 4096), (1000, 2064), (6144, 144)])
 def test_decode_batch_shapes(oracle_mod, M, N, K):
     x = workloads.gaussian_outliers(M, K, 41 + M, DEV)
     w = workloads.weights(N, K, 41, DEV)
+    layer(oracle_mod, x, w)
+
+
+# One token with long rows: 32 to 64 k-blocks per CTA at eight K-splits,
+# with and without a ragged last k-block.
+@pytest.mark.parametrize("K", [4096, 28672, 32768, 32784, 65536])
+def test_single_token_long_rows(oracle_mod, K):
+    x = workloads.gaussian_outliers(1, K, 43, DEV)
+    w = workloads.weights(256, K, 43, DEV)
     layer(oracle_mod, x, w)
 
 
