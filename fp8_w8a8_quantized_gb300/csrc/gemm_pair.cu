@@ -214,57 +214,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;
         const int row_in_tile = static_cast<int>(rank) * (BM / 2) + quarter * 32 + lane;
         const bool vec_ok = (N % 8) == 0;
-        const bool sw_vec = (reinterpret_cast<uintptr_t>(s_w) & 15u) == 0;
         int local = 0;
         for (int t = pair; t < tiles; t += pairs, ++local) {
             int m_blk, n_blk;
             tile_coords(t, num_m, num_n, m_blk, n_blk);
             const int buf = local % kAccBufs;
             const uint32_t acc_phase = (local / kAccBufs) & 1;
-            if (!warp_wait(&bars->acc_full[buf], acc_phase, abort_flag, status)) break;
-            tc_fence_after();
             const int m = m_blk * BM + row_in_tile;
             const bool row_ok = m < M;
+            // The tile's scales, loaded before its accumulator is ready: the
+            // token scale of this lane's row, and in swl[c] the weight scale
+            // of column c * 32 + lane (broadcast to the warp by shuffles).
             const float st = row_ok ? __ldg(s_tok + m) : 0.0f;
+            float swl[BN / 32];
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                const int n = n_blk * BN + c * 32 + lane;
+                swl[c] = n < N ? __ldg(s_w + n) : 0.0f;
+            }
+            if (!warp_wait(&bars->acc_full[buf], acc_phase, abort_flag, status)) break;
+            tc_fence_after();
             const uint32_t tbase =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN;
             __nv_bfloat16* yrow = y + static_cast<int64_t>(row_ok ? m : 0) * N;
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tbase + c * 32, r);
-                tmem_ld_wait();
-                if (c == BN / 32 - 1) {
-                    // accumulator read: return the buffer to the even CTA's MMA warp
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive_cluster(map_to_rank(smem_u32(&bars->acc_empty[buf]), 0));
+            // 32 columns: scale, round to bf16, store (16-byte stores when the
+            // row is 16-byte aligned and the chunk is whole).
+            auto store_chunk = [&](const uint32_t (&r)[32], float sw_lane, int c) {
+                uint32_t packed[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float s0 = __shfl_sync(0xFFFFFFFFu, sw_lane, 2 * j);
+                    const float s1 = __shfl_sync(0xFFFFFFFFu, sw_lane, 2 * j + 1);
+                    const float v0 = (__uint_as_float(r[2 * j]) * st) * s0;
+                    const float v1 = (__uint_as_float(r[2 * j + 1]) * st) * s1;
+                    packed[j] = pack_bf16x2(v0, v1);
                 }
                 const int n0 = n_blk * BN + c * 32;
                 if (row_ok && n0 < N) {
-                    float sw[32];
-                    if (sw_vec && n0 + 32 <= N) {
-                        const float4* p = reinterpret_cast<const float4*>(s_w + n0);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float4 v = __ldg(p + j);
-                            sw[4 * j] = v.x;
-                            sw[4 * j + 1] = v.y;
-                            sw[4 * j + 2] = v.z;
-                            sw[4 * j + 3] = v.w;
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) sw[j] = n0 + j < N ? __ldg(s_w + n0 + j) : 0.0f;
-                    }
-                    uint32_t packed[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float v0 = (__uint_as_float(r[2 * j]) * st) * sw[2 * j];
-                        const float v1 = (__uint_as_float(r[2 * j + 1]) * st) * sw[2 * j + 1];
-                        packed[j] = pack_bf16x2(v0, v1);
-                    }
                     if (vec_ok && n0 + 32 <= N) {
                         uint4* dst = reinterpret_cast<uint4*>(yrow + n0);
 #pragma unroll
@@ -277,8 +263,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                             dst[j] = static_cast<uint16_t>(packed[j >> 1] >> ((j & 1) * 16));
                     }
                 }
-                __syncwarp();
+            };
+            // TMEM loads double-buffered: chunk c + 1 is in flight while
+            // chunk c is scaled and stored.
+            uint32_t ra[32], rb[32];
+            tmem_ld_32x32b_x32(tbase, ra);
+            tmem_ld_wait_regs(ra);
+#pragma unroll
+            for (int c = 0; c < BN / 32; c += 2) {
+                tmem_ld_32x32b_x32(tbase + (c + 1) * 32, rb);
+                store_chunk(ra, swl[c], c);
+                tmem_ld_wait_regs(rb);
+                if (c + 2 < BN / 32) {
+                    tmem_ld_32x32b_x32(tbase + (c + 2) * 32, ra);
+                } else {
+                    // accumulator read: return the buffer to the even CTA's MMA warp
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive_cluster(map_to_rank(smem_u32(&bars->acc_empty[buf]), 0));
+                }
+                store_chunk(rb, swl[c + 1], c + 1);
+                if (c + 2 < BN / 32) tmem_ld_wait_regs(ra);
             }
+            __syncwarp();
         }
     }
 
