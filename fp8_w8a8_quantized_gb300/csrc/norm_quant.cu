@@ -139,8 +139,8 @@ __global__ void __launch_bounds__(G > kBlock ? G : kBlock)
     for (int i = 0; i < VPT; ++i) {
         const int64_t c = t + static_cast<int64_t>(i) * G;
         if (c < C) {
-            const uint2 a = quant8(v[i][0], dv);
-            const uint2 b = quant8(v[i][1], dv);
+            const uint2 a = quant8<true>(v[i][0], dv);
+            const uint2 b = quant8<true>(v[i][1], dv);
             qr[c] = make_uint4(a.x, a.y, b.x, b.y);
             if (yr) {
                 yr[2 * c] = v[i][0];

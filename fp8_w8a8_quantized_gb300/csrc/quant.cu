@@ -113,8 +113,8 @@ __global__ void __launch_bounds__(G > kBlock ? G : kBlock)
     for (int i = 0; i < VPT; ++i) {
         const int64_t c = t + static_cast<int64_t>(i) * G;
         if (c < C) {
-            const uint2 a = quant8(v[i][0], dv);
-            const uint2 b = quant8(v[i][1], dv);
+            const uint2 a = quant8<true>(v[i][0], dv);
+            const uint2 b = quant8<true>(v[i][1], dv);
             qr[c] = make_uint4(a.x, a.y, b.x, b.y);
         }
     }
@@ -142,8 +142,8 @@ __global__ void __launch_bounds__(1024)
     const Divisor dv = divisor_of(sc);
     uint4* qr = reinterpret_cast<uint4*>(q + row * ldq);
     for (int64_t c = threadIdx.x; c < C; c += 1024) {
-        const uint2 a = quant8(ld_stream(xr + 2 * c), dv);
-        const uint2 b = quant8(ld_stream(xr + 2 * c + 1), dv);
+        const uint2 a = quant8<true>(ld_stream(xr + 2 * c), dv);
+        const uint2 b = quant8<true>(ld_stream(xr + 2 * c + 1), dv);
         qr[c] = make_uint4(a.x, a.y, b.x, b.y);
     }
     if (threadIdx.x == 0) s[row] = sc;

@@ -11,6 +11,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "ptx.cuh"
+
 namespace fp8k {
 
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
@@ -20,8 +22,19 @@ __device__ __forceinline__ float amax2(uint32_t u, float m) {
     return fmaxf(fmaxf(m, fabsf(bf16lo(u))), fabsf(bf16hi(u)));
 }
 
+// max(|a|, |b|) per bf16 lane (exact); the sign bits of the result are
+// the XOR of the inputs' and carry no meaning.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// max(m, |x_0|, ..., |x_7|) over eight bf16 values, exact: the maxima are
+// taken on bf16 pairs, then the two lanes are widened (exactly) to fp32.
 __device__ __forceinline__ float amax8(const uint4& v, float m) {
-    return amax2(v.w, amax2(v.z, amax2(v.y, amax2(v.x, m))));
+    const uint32_t a = absmax_bf16x2(absmax_bf16x2(v.x, v.y), absmax_bf16x2(v.z, v.w)) & 0x7FFF7FFFu;
+    return fmaxf(m, fmaxf(bf16lo(a), bf16hi(a)));
 }
 
 // Two fp32 values -> two E4M3 codes (RN, saturating to +-448); `lo` lands in
@@ -46,13 +59,14 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
 // scale whose reciprocal is not a normal number (s below the normal range or
 // above 2^126), or that is not finite, takes the IEEE division.
 struct Divisor {
-    float s, r;
+    float s, ns, r;  // s, -s, RN(1/s)
     bool ieee;
 };
 
 __device__ __forceinline__ Divisor divisor_of(float s) {
     Divisor d;
     d.s = s;
+    d.ns = -s;
     d.r = __frcp_rn(s);
     d.ieee = !(s >= 1.17549435e-38f && s <= 8.50705917e37f);  // [2^-126, 2^126]
     return d;
@@ -66,9 +80,29 @@ __device__ __forceinline__ float div_rn(float x, const Divisor& d) {
     return isinf(q0) ? q0 : q;
 }
 
-// One bf16 pair -> two codes in the low 16 bits.
+// One bf16 pair -> two codes in the low 16 bits: div_rn on both values in
+// packed f32x2 fused multiply-adds (each lane an IEEE fp32 FMA, so the same
+// bits).  q0 = RN(x * r) is formed as RN(x * r + (-0)), which equals the
+// product's rounding for every x, signed zeros included.  kBounded: the
+// scale comes from these values' own maximum (s = amax / 448), so |q0| stays
+// near 448 and cannot overflow; otherwise an infinite q0 is kept, as in
+// div_rn.
+template <bool kBounded>
 __device__ __forceinline__ uint32_t quant2(uint32_t u, const Divisor& d) {
-    return cvt_e4m3x2(div_rn(bf16lo(u), d), div_rn(bf16hi(u), d));
+    const float x0 = bf16lo(u), x1 = bf16hi(u);
+    float q0 = -0.0f, q1 = -0.0f;
+    fma2(q0, q1, x0, x1, d.r, d.r);
+    float e0 = x0, e1 = x1;
+    fma2(e0, e1, q0, q1, d.ns, d.ns);  // x - s * q0, exact
+    float y0 = q0, y1 = q1;
+    fma2(y0, y1, e0, e1, d.r, d.r);
+    y0 = copysignf(y0, x0);
+    y1 = copysignf(y1, x1);
+    if (!kBounded) {
+        y0 = isinf(q0) ? q0 : y0;
+        y1 = isinf(q1) ? q1 : y1;
+    }
+    return cvt_e4m3x2(y0, y1);
 }
 
 __device__ __forceinline__ uint32_t quant2_ieee(uint32_t u, float s) {
@@ -83,10 +117,12 @@ static __device__ __noinline__ uint2 quant8_ieee(uint4 v, float s) {
 }
 
 // Eight bf16 values (16 bytes) -> eight codes packed in two 32-bit words.
+// kBounded as for quant2: true where s = amax / 448 of a set holding v.
+template <bool kBounded = false>
 __device__ __forceinline__ uint2 quant8(const uint4& v, const Divisor& d) {
     if (d.ieee) return quant8_ieee(v, d.s);
-    return make_uint2(quant2(v.x, d) | (quant2(v.y, d) << 16),
-                      quant2(v.z, d) | (quant2(v.w, d) << 16));
+    return make_uint2(quant2<kBounded>(v.x, d) | (quant2<kBounded>(v.y, d) << 16),
+                      quant2<kBounded>(v.z, d) | (quant2<kBounded>(v.w, d) << 16));
 }
 
 __device__ __forceinline__ float scale_of(float amax) {

@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kThreads)
         const float sc = scale_of(m);
         if (live) {
             const Divisor dv = divisor_of(sc);
-            const uint2 qa = quant8(a, dv), qb = quant8(b, dv);
+            const uint2 qa = quant8<true>(a, dv), qb = quant8<true>(b, dv);
             *reinterpret_cast<uint4*>(q + r * ldq + k) = make_uint4(qa.x, qa.y, qb.x, qb.y);
             if (sub == 0) s[r * KB + kb] = sc;
         }
@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(kThreads)
     for (int i = 0; i < 4; ++i) {
         const int64_t n = nb * kGroup + (threadIdx.x >> 3) + 32 * i;
         if (n < N && k < K) {
-            const uint2 qa = quant8(v[i][0], dv), qb = quant8(v[i][1], dv);
+            const uint2 qa = quant8<true>(v[i][0], dv), qb = quant8<true>(v[i][1], dv);
             *reinterpret_cast<uint4*>(q + n * ldq + k) = make_uint4(qa.x, qa.y, qb.x, qb.y);
         }
     }
