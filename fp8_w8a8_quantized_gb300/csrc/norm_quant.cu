@@ -69,22 +69,24 @@ __device__ __forceinline__ uint16_t bf16_bits(float f) {
 }
 
 // One bf16 pair normalised (x * inv * g, each product rounded to fp32, then
-// bf16); the running max |y| is updated.
-__device__ __forceinline__ uint32_t norm2(uint32_t xw, uint32_t gw, float inv, float& m) {
-    const float lo = __fmul_rn(__fmul_rn(bf16lo(xw), inv), bf16lo(gw));
-    const float hi = __fmul_rn(__fmul_rn(bf16hi(xw), inv), bf16hi(gw));
-    const uint32_t y = static_cast<uint32_t>(bf16_bits(lo)) | (static_cast<uint32_t>(bf16_bits(hi)) << 16);
-    m = amax2(y, m);
-    return y;
+// bf16).  The products are packed f32x2 fused multiply-adds with a -0
+// addend: RN(a * b + (-0)) is RN(a * b) for every a, b, signed zeros
+// included.
+__device__ __forceinline__ uint32_t norm2(uint32_t xw, uint32_t gw, float inv) {
+    float lo = -0.0f, hi = -0.0f;
+    fma2(lo, hi, bf16lo(xw), bf16hi(xw), inv, inv);
+    float ylo = -0.0f, yhi = -0.0f;
+    fma2(ylo, yhi, lo, hi, bf16lo(gw), bf16hi(gw));
+    return static_cast<uint32_t>(bf16_bits(ylo)) | (static_cast<uint32_t>(bf16_bits(yhi)) << 16);
 }
 
 // Normalise 8 values in place; returns the running max |y|.
 __device__ __forceinline__ float norm8(uint4& v, const uint4& g, float inv, float m) {
-    v.x = norm2(v.x, g.x, inv, m);
-    v.y = norm2(v.y, g.y, inv, m);
-    v.z = norm2(v.z, g.z, inv, m);
-    v.w = norm2(v.w, g.w, inv, m);
-    return m;
+    v.x = norm2(v.x, g.x, inv);
+    v.y = norm2(v.y, g.y, inv);
+    v.z = norm2(v.z, g.z, inv);
+    v.w = norm2(v.w, g.w, inv);
+    return amax8(v, m);
 }
 
 template <int G, int VPT>

@@ -27,14 +27,16 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int64_t kGroup = 128;  // block edge of the block-wise scales
 
+template <bool kBounded = false>
 __device__ __forceinline__ uint4 quant16(const uint4* src, const Divisor& d) {
     const uint4 a = __ldg(src), b = __ldg(src + 1);
-    const uint2 qa = quant8(a, d), qb = quant8(b, d);
+    const uint2 qa = quant8<kBounded>(a, d), qb = quant8<kBounded>(b, d);
     return make_uint4(qa.x, qa.y, qb.x, qb.y);
 }
 
 // x [R, K] (ld ldx elements) / s -> q [R, K] (ld ldq bytes), grid-stride
-// over 16-element chunks.
+// over 16-element chunks.  kBounded: s = amax / 448 of x itself.
+template <bool kBounded = false>
 __device__ __forceinline__ void quant_chunks(const uint16_t* __restrict__ x, int64_t R, int64_t K,
                                              int64_t ldx, float s, uint8_t* __restrict__ q,
                                              int64_t ldq) {
@@ -45,7 +47,7 @@ __device__ __forceinline__ void quant_chunks(const uint16_t* __restrict__ x, int
          i += static_cast<int64_t>(gridDim.x) * kThreads) {
         const int64_t r = i / C, c = i - r * C;
         const uint4* src = reinterpret_cast<const uint4*>(x + r * ldx + c * 16);
-        *reinterpret_cast<uint4*>(q + r * ldq + c * 16) = quant16(src, dv);
+        *reinterpret_cast<uint4*>(q + r * ldq + c * 16) = quant16<kBounded>(src, dv);
     }
 }
 
@@ -113,7 +115,7 @@ __global__ void __launch_bounds__(kThreads)
     for (int i = threadIdx.x; i < n_partial; i += kThreads) m = fmaxf(m, partial[i]);
     const float s = scale_of(block_max(m, red));
     if (blockIdx.x == 0 && threadIdx.x == 0) *s_out = s;
-    quant_chunks(x, R, K, ldx, s, q, ldq);
+    quant_chunks<true>(x, R, K, ldx, s, q, ldq);
     if (s_rows) fill_rows(s_rows, R, s);
 }
 
