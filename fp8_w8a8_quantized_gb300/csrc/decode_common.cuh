@@ -164,6 +164,39 @@ __device__ __forceinline__ void push_reduce(const float* recv, int splits, int l
 template <int S, typename Out>
 __device__ __forceinline__ void pull_reduce_s(const float* red, int lo, int width, int M,
                                               Out out) {
+    constexpr int kRowsPer = (BNW + S - 1) / S;
+    if constexpr (kRowsPer % 4 == 0) {
+        // Every owner's rows start on a multiple of 4 (S = 1, 2, 4, 8): an
+        // item is 4 consecutive rows of one token, one 16-byte load per
+        // peer (a quarter of the remote requests), summed in rank order
+        // lane by lane -- the same sums as one row at a time.
+        const int groups = width / 4;
+        const int items = groups * M;
+        uint32_t peer[S];
+#pragma unroll
+        for (int j = 0; j < S; ++j) peer[j] = map_to_rank(smem_u32(red), j);
+        for (int i = static_cast<int>(threadIdx.x); i < items; i += kThreads) {
+            const int m = i / groups;
+            const int r = lo + 4 * (i - m * groups);
+            const uint32_t off = static_cast<uint32_t>((m * BNW + r) * 4);
+            float4 part[S];
+#pragma unroll
+            for (int j = 0; j < S; ++j) part[j] = ld_dsmem_v4(peer[j] + off);
+            float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+#pragma unroll
+            for (int j = 0; j < S; ++j) {
+                a0 += part[j].x;
+                a1 += part[j].y;
+                a2 += part[j].z;
+                a3 += part[j].w;
+            }
+            out(m, r, a0);
+            out(m, r + 1, a1);
+            out(m, r + 2, a2);
+            out(m, r + 3, a3);
+        }
+        return;
+    }
     constexpr int kItems = S == 1 ? 16 : 32 / S;
     const int items = width * M;
     uint32_t peer[S];
