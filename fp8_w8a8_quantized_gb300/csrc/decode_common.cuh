@@ -84,11 +84,20 @@ inline int choose_splits(int n_tiles, int nk, int num_sms, const int* clusters =
 // ---------------------------------------------------------------------------
 // Split-K reduction.  Each CTA of a cluster of S owns output rows
 // [lo, lo + width) of the 128-row slab, lo = rank * rows_per with rows_per =
-// ceil(128 / S), and sums the S partials of those rows in rank order
+// owner_rows(S) (ceil(128 / S) rounded up to a multiple of 4), and sums the
+// S partials of those rows in rank order
 // (deterministic).  `out(m, r, sum)` writes the output of token m, slab row
 // r.  Outputs are visited token-major (item i = token i / width, row lo +
 // i % width), so a warp writes consecutive outputs of one token.
 // ---------------------------------------------------------------------------
+
+// Output rows owned by each CTA of a cluster of S: ceil(128 / S) rounded
+// up to a multiple of 4, so every owner's rows start on a 16-byte boundary
+// of a token's partial row (the last owner takes what is left: 8 to 128
+// rows, never none).
+__host__ __device__ __forceinline__ int owner_rows(int splits) {
+    return ((BNW + splits - 1) / splits + 3) & ~3;
+}
 
 // Push: the partials arrive in a receive buffer of this CTA laid out
 // [S][rows_per][stride] fp32 (stride = Mp + 4, Mp = M rounded up to 4: the
@@ -96,7 +105,7 @@ inline int choose_splits(int n_tiles, int nk, int num_sms, const int* clusters =
 __host__ __device__ __forceinline__ int push_stride(int M) { return ((M + 3) & ~3) + 4; }
 
 __host__ __device__ __forceinline__ uint32_t push_recv_bytes(int M, int splits) {
-    const int rows_per = (BNW + splits - 1) / splits;
+    const int rows_per = owner_rows(splits);
     return (static_cast<uint32_t>(splits * rows_per * push_stride(M) * 4) + 127u) & ~127u;
 }
 
@@ -110,7 +119,7 @@ __device__ __forceinline__ uint32_t push_expect_bytes(int M, int splits, int wid
 template <int MT>
 __device__ __forceinline__ void push_send(const float (&v)[MT], int M, int nl, uint32_t rank,
                                           int splits, float* recv, uint64_t* recv_full) {
-    const int rows_per = (BNW + splits - 1) / splits;
+    const int rows_per = owner_rows(splits);
     const int owner = nl / rows_per;
     const int rloc = nl - owner * rows_per;
     const uint32_t dst =
@@ -129,7 +138,7 @@ template <typename Out>
 __device__ __forceinline__ void push_reduce(const float* recv, int splits, int lo, int width,
                                             int M, Out out) {
     if (width <= 0) return;
-    const int rows_per = (BNW + splits - 1) / splits;
+    const int rows_per = owner_rows(splits);
     const int stride = push_stride(M);
     const int split_step = rows_per * stride;
     // walk i = threadIdx.x, +kThreads, ... as (m, r) without dividing
@@ -164,12 +173,12 @@ __device__ __forceinline__ void push_reduce(const float* recv, int splits, int l
 template <int S, typename Out>
 __device__ __forceinline__ void pull_reduce_s(const float* red, int lo, int width, int M,
                                               Out out) {
-    constexpr int kRowsPer = (BNW + S - 1) / S;
+    constexpr int kRowsPer = ((BNW + S - 1) / S + 3) & ~3;  // owner_rows(S)
     if constexpr (kRowsPer % 4 == 0) {
-        // Every owner's rows start on a multiple of 4 (S = 1, 2, 4, 8): an
-        // item is 4 consecutive rows of one token, one 16-byte load per
-        // peer (a quarter of the remote requests), summed in rank order
-        // lane by lane -- the same sums as one row at a time.
+        // Every owner's rows start on a multiple of 4 (owner_rows): an item
+        // is 4 consecutive rows of one token, one 16-byte load per peer (a
+        // quarter of the remote requests), summed in rank order lane by
+        // lane -- the same sums as one row at a time.
         const int groups = width / 4;
         const int items = groups * M;
         uint32_t peer[S];

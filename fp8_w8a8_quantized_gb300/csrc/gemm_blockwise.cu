@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kThreads)
     const int kb0 = static_cast<int>(rank) * per + min(static_cast<int>(rank), rem);
     const int nkb = per + (static_cast<int>(rank) < rem ? 1 : 0);
     // output rows [lo, hi) of the slab are reduced and stored by this CTA
-    const int rows_per = (BNW + splits - 1) / splits;
+    const int rows_per = owner_rows(splits);
     const int lo = static_cast<int>(rank) * rows_per;
     const int hi = min(BNW, lo + rows_per);
     const int width = hi > lo ? hi - lo : 0;

@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kThreads)
     int kb0, nkb;
     split_range(static_cast<int>(rank), nk, splits, &kb0, &nkb);
     // output rows [lo, hi) of the slab are reduced and stored by this CTA
-    const int rows_per = (BNW + splits - 1) / splits;
+    const int rows_per = owner_rows(splits);
     const int lo = static_cast<int>(rank) * rows_per;
     const int hi = min(BNW, lo + rows_per);
     const int width = hi > lo ? hi - lo : 0;
