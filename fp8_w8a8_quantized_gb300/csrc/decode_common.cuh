@@ -95,7 +95,7 @@ inline int choose_splits(int n_tiles, int nk, int num_sms, const int* clusters =
 // up to a multiple of 4, so every owner's rows start on a 16-byte boundary
 // of a token's partial row (the last owner takes what is left: 8 to 128
 // rows, never none).
-__host__ __device__ __forceinline__ int owner_rows(int splits) {
+__host__ __device__ constexpr int owner_rows(int splits) {
     return ((BNW + splits - 1) / splits + 3) & ~3;
 }
 
@@ -165,73 +165,41 @@ __device__ __forceinline__ void push_reduce(const float* recv, int splits, int l
 }
 
 // Pull: every CTA left its partial D^T tile [MT][BNW] at `red`; after a
-// cluster barrier each owner reads the S partials of its rows.  A thread
-// takes kItems items per round and issues all their S loads before summing
-// any (about 32 loads in flight), so each round costs one distributed-
-// shared-memory round trip.  A second cluster barrier must keep every CTA
-// alive until its peers have read it.
+// cluster barrier each owner reads the S partials of its rows.  Owners hold
+// multiples of 4 rows starting on a multiple of 4 (owner_rows), so an item
+// is 4 consecutive rows of one token: one 16-byte load per peer, all S
+// loads issued before any sum (one distributed-shared-memory round trip),
+// then the 4 lanes summed in rank order -- the same sums as one row at a
+// time.  A second cluster barrier must keep every CTA alive until its peers
+// have read it.
 template <int S, typename Out>
 __device__ __forceinline__ void pull_reduce_s(const float* red, int lo, int width, int M,
                                               Out out) {
-    constexpr int kRowsPer = ((BNW + S - 1) / S + 3) & ~3;  // owner_rows(S)
-    if constexpr (kRowsPer % 4 == 0) {
-        // Every owner's rows start on a multiple of 4 (owner_rows): an item
-        // is 4 consecutive rows of one token, one 16-byte load per peer (a
-        // quarter of the remote requests), summed in rank order lane by
-        // lane -- the same sums as one row at a time.
-        const int groups = width / 4;
-        const int items = groups * M;
-        uint32_t peer[S];
-#pragma unroll
-        for (int j = 0; j < S; ++j) peer[j] = map_to_rank(smem_u32(red), j);
-        for (int i = static_cast<int>(threadIdx.x); i < items; i += kThreads) {
-            const int m = i / groups;
-            const int r = lo + 4 * (i - m * groups);
-            const uint32_t off = static_cast<uint32_t>((m * BNW + r) * 4);
-            float4 part[S];
-#pragma unroll
-            for (int j = 0; j < S; ++j) part[j] = ld_dsmem_v4(peer[j] + off);
-            float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-#pragma unroll
-            for (int j = 0; j < S; ++j) {
-                a0 += part[j].x;
-                a1 += part[j].y;
-                a2 += part[j].z;
-                a3 += part[j].w;
-            }
-            out(m, r, a0);
-            out(m, r + 1, a1);
-            out(m, r + 2, a2);
-            out(m, r + 3, a3);
-        }
-        return;
-    }
-    constexpr int kItems = S == 1 ? 16 : 32 / S;
-    const int items = width * M;
+    static_assert(owner_rows(S) % 4 == 0, "owners hold whole 4-row groups");
+    const int groups = width / 4;  // width: owner_rows(S), or the last owner's rest
+    const int items = groups * M;
     uint32_t peer[S];
 #pragma unroll
     for (int j = 0; j < S; ++j) peer[j] = map_to_rank(smem_u32(red), j);
-    for (int i0 = static_cast<int>(threadIdx.x); i0 < items; i0 += kThreads * kItems) {
-        float part[kItems][S];
+    for (int i = static_cast<int>(threadIdx.x); i < items; i += kThreads) {
+        const int m = i / groups;
+        const int r = lo + 4 * (i - m * groups);
+        const uint32_t off = static_cast<uint32_t>((m * BNW + r) * 4);
+        float4 part[S];
 #pragma unroll
-        for (int p = 0; p < kItems; ++p) {
-            const int i = i0 + p * kThreads;
-            const int m = i / width;
-            const uint32_t off = static_cast<uint32_t>((m * BNW + lo + (i - m * width)) * 4);
+        for (int j = 0; j < S; ++j) part[j] = ld_dsmem_v4(peer[j] + off);
+        float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
 #pragma unroll
-            for (int j = 0; j < S; ++j) part[p][j] = i < items ? ld_dsmem_f32(peer[j] + off) : 0.0f;
+        for (int j = 0; j < S; ++j) {
+            a0 += part[j].x;
+            a1 += part[j].y;
+            a2 += part[j].z;
+            a3 += part[j].w;
         }
-#pragma unroll
-        for (int p = 0; p < kItems; ++p) {
-            const int i = i0 + p * kThreads;
-            if (i < items) {
-                const int m = i / width;
-                float acc = 0.0f;
-#pragma unroll
-                for (int j = 0; j < S; ++j) acc += part[p][j];
-                out(m, lo + (i - m * width), acc);
-            }
-        }
+        out(m, r, a0);
+        out(m, r + 1, a1);
+        out(m, r + 2, a2);
+        out(m, r + 3, a3);
     }
 }
 
