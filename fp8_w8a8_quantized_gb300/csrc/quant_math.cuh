@@ -18,10 +18,6 @@ namespace fp8k {
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 
-__device__ __forceinline__ float amax2(uint32_t u, float m) {
-    return fmaxf(fmaxf(m, fabsf(bf16lo(u))), fabsf(bf16hi(u)));
-}
-
 // max(|a|, |b|) per bf16 lane (exact); the sign bits of the result are
 // the XOR of the inputs' and carry no meaning.
 __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
@@ -72,7 +68,8 @@ __device__ __forceinline__ Divisor divisor_of(float s) {
     return d;
 }
 
-// RN(x / s) for a scale on the fast path (d.ieee false).
+// RN(x / s) for a scale on the fast path (d.ieee false): the method for one
+// value; quant2 below runs it on two values per instruction.
 __device__ __forceinline__ float div_rn(float x, const Divisor& d) {
     const float q0 = __fmul_rn(x, d.r);
     const float e = __fmaf_rn(-q0, d.s, x);
