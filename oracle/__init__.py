@@ -8,9 +8,11 @@ with gcc, no fast-math), and this module only marshals numpy arrays.
 
 What it computes (page title, section):
 
-* E4M3 codec and the ``round_e4m3`` semantics -- "FP8 Inference Explained, in
-  depth", "The numbers in one byte"; bit layout from "FP8 Quantization",
-  "FP8 Representation".
+* E4M3 codec -- "FP8 Inference Explained, in depth", "The numbers in one
+  byte"; bit layout from "FP8 Quantization", "FP8 Representation".  A value
+  is encoded as the nearest entry of the decoded code table (ties to the even
+  code, saturating at +-448); a test checks that this equals the pages'
+  step-by-step rounding (binade, grid spacing, half to even, clip).
 * Per-token dynamic quantization, s = amax/448, q = E4M3(fl32(x / s)) --
   "FP8 Inference Explained", "Scales and their granularity"; "Quantization:
   FP8 inference and KV-cache quantization", "Dynamic scales or static scales".
@@ -131,8 +133,8 @@ def e4m3_decode(codes) -> np.ndarray:
 
 
 def round_e4m3(values) -> np.ndarray:
-    """The pages' round_e4m3: nearest E4M3 value (fp64), ties to even,
-    saturating at +-448, zero and NaN unchanged."""
+    """Nearest E4M3 value (fp64), ties to even, saturating at +-448, zero
+    and NaN unchanged (the decoded code of e4m3_encode)."""
     lib = _load()
     v = np.asarray(values, dtype=np.float64)
     return np.array([lib.orc_round_e4m3(float(x)) for x in v.ravel()],

@@ -65,45 +65,56 @@ double orc_e4m3_decode(uint8_t c)
     return sign ? -v : v;
 }
 
-/* Round-half-to-even of a non-negative double that is exactly representable
- * (the caller divides by a power of two, so no rounding has happened yet). */
-static double round_half_even(double t)
+/* Saturating round-to-nearest-even conversion to E4M3, derived from the
+ * code table itself rather than from exponent arithmetic.
+ * [P2 "The numbers in one byte"] fixes the grid (the decoded codes above),
+ * the rounding (to the nearest representable value, halfway cases to the
+ * even one, as Python's round does) and the saturation at +-448; [P4
+ * "Dynamic scales or static scales"] the saturating (not NaN) overflow.
+ * The positive finite codes 0x00..0x7E decode to strictly increasing
+ * values, so the two codes that bracket |x| are found by bisection on the
+ * code number; the closer one wins, and on an exact tie the one with an even
+ * mantissa field, which is the even code number (the mantissa is the low
+ * three bits).  Distances are exact: |x| and both bracketing values are
+ * dyadic numbers well inside the range of a double.  The sign of x (zero
+ * included) becomes bit 7. */
+uint8_t orc_e4m3_encode(double x)
 {
-    double f = floor(t);
-    double d = t - f;
-    if (d > 0.5)
-        return f + 1.0;
-    if (d < 0.5)
-        return f;
-    return (fmod(f, 2.0) == 0.0) ? f : f + 1.0;
+    uint8_t sign;
+    double a, d_lo, d_hi;
+    int lo, hi;
+    if (isnan(x))
+        return 0x7F;
+    sign = signbit(x) ? 0x80 : 0x00;
+    a = fabs(x);
+    if (a >= E4M3_MAX)
+        return (uint8_t)(sign | 0x7E);
+    /* invariant: decode(lo) <= a < decode(hi) */
+    lo = 0x00;
+    hi = 0x7E;
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (orc_e4m3_decode((uint8_t)mid) <= a)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    d_lo = a - orc_e4m3_decode((uint8_t)lo);
+    d_hi = orc_e4m3_decode((uint8_t)hi) - a;
+    if (d_lo < d_hi)
+        return (uint8_t)(sign | lo);
+    if (d_hi < d_lo)
+        return (uint8_t)(sign | hi);
+    return (uint8_t)(sign | ((lo % 2 == 0) ? lo : hi));
 }
 
-/* The pages' round_e4m3 semantics [P2 "The numbers in one byte"]:
- *   zero and NaN pass through; otherwise keep the sign, clamp |x| to 448,
- *   take the binade exponent e = max(floor(log2 |x|), -6) (-6 is the
- *   smallest normal exponent, so below 2^-6 the step stays 2^-9), quantize
- *   with step 2^(e-3) (three mantissa bits) rounding half to even, and clamp
- *   to 448 again.
- * floor(log2 a) is taken from frexp, which is exact, instead of a floating
- * point log2. */
+/* The E4M3 value nearest to x (ties to even, saturating at +-448), as a
+ * double: the decoded code.  Zero (either sign) and NaN pass through. */
 double orc_round_e4m3(double x)
 {
-    double a, step, q;
-    int ex, e;
     if (x == 0.0 || isnan(x))
         return x;
-    a = fabs(x);
-    if (a > E4M3_MAX)
-        a = E4M3_MAX;
-    frexp(a, &ex);            /* a = f * 2^ex with f in [0.5, 1) */
-    e = ex - 1;               /* floor(log2 a) */
-    if (e < -6)
-        e = -6;
-    step = ldexp(1.0, e - 3);
-    q = round_half_even(a / step) * step;
-    if (q > E4M3_MAX)
-        q = E4M3_MAX;
-    return copysign(q, x);
+    return orc_e4m3_decode(orc_e4m3_encode(x));
 }
 
 /* Bit pattern of a value that is already on the E4M3 grid (the output of
@@ -128,13 +139,6 @@ uint8_t orc_e4m3_pack(double v)
     return (uint8_t)(sign | (E << 3) | m);
 }
 
-/* Saturating, round-to-nearest-even conversion of a real value to E4M3. */
-uint8_t orc_e4m3_encode(double x)
-{
-    if (isnan(x))
-        return 0x7F;
-    return orc_e4m3_pack(orc_round_e4m3(x));
-}
 
 /* ------------------------------------------------------------------------ */
 /* Dynamic per-token (and per-output-channel) quantization                  */

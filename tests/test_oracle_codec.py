@@ -135,3 +135,38 @@ def test_known_codes(oracle_mod, code):
     expect = {0x38: 1.0, 0x39: 1.125, 0x01: 2.0 ** -9, 0x08: 2.0 ** -6,
               0x7E: 448.0, 0xB8: -1.0, 0xFE: -448.0}[code]
     assert oracle_mod.e4m3_decode([code])[0] == expect
+
+
+def stepwise_round(x: float) -> float:
+    """The rounding as the pages state it step by step ("FP8 Inference
+    Explained, in depth", "The numbers in one byte"): keep the sign, clip
+    the magnitude at 448, find its binade 2^e with e no lower than -6 (the
+    smallest normal exponent; below it the spacing stays 2^-9), snap to the
+    binade's grid of spacing 2^(e-3) with halfway cases to even, clip again.
+    Written independently of the oracle, which instead picks the nearest
+    entry of the decoded code table; the two must agree everywhere."""
+    if x == 0.0 or math.isnan(x):
+        return x
+    a = min(abs(x), 448.0)
+    e = max(math.frexp(a)[1] - 1, -6)
+    step = 2.0 ** (e - 3)
+    r = min(round(a / step) * step, 448.0)   # Python's round: half to even
+    return math.copysign(r, x)
+
+
+def test_table_rounding_equals_stepwise_rounding(oracle_mod):
+    grid = oracle_mod.e4m3_decode(np.array(list(range(0x7F)), dtype=np.uint8))
+    pts = list(grid)
+    for lo, hi in zip(grid[:-1], grid[1:]):
+        mid = (lo + hi) / 2.0
+        pts += [mid, float(np.nextafter(mid, 0.0)), float(np.nextafter(mid, np.inf)),
+                lo + (hi - lo) / 4.0, hi - (hi - lo) / 8.0]
+    rng = np.random.default_rng(99)
+    pts += list(np.exp2(rng.uniform(-20.0, 12.0, 20000)))
+    pts += [2.0 ** -10, 3 * 2.0 ** -10, 1e-30, 447.9, 448.0, 455.99, 456.0, 464.0, 1e6]
+    vals = np.array(pts + [-p for p in pts], dtype=np.float64)
+    ours = oracle_mod.round_e4m3(vals)
+    ref = np.array([stepwise_round(float(v)) for v in vals])
+    bad = np.nonzero(ours != ref)[0]
+    assert bad.size == 0, [(vals[i], ours[i], ref[i]) for i in bad[:5]]
+    assert np.array_equal(np.signbit(ours), np.signbit(ref))
