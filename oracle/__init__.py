@@ -55,7 +55,7 @@ def build(force: bool = False) -> str:
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off",
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-pthread", "-ffp-contract=off",
            "-fno-fast-math", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)

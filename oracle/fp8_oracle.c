@@ -33,6 +33,7 @@
  * No -ffast-math: every fp32 division below must be IEEE.
  */
 #include <math.h>
+#include <pthread.h>
 #include <stdint.h>
 #include <string.h>
 #ifdef _OPENMP
@@ -78,11 +79,22 @@ double orc_e4m3_decode(uint8_t c)
  * three bits).  Distances are exact: |x| and both bracketing values are
  * dyadic numbers well inside the range of a double.  The sign of x (zero
  * included) becomes bit 7. */
+static double g_grid[0x7F];          /* g_grid[c] = orc_e4m3_decode(c), c = 0..0x7E */
+static pthread_once_t g_grid_once = PTHREAD_ONCE_INIT;
+
+static void fill_grid(void)
+{
+    int c;
+    for (c = 0; c < 0x7F; ++c)
+        g_grid[c] = orc_e4m3_decode((uint8_t)c);
+}
+
 uint8_t orc_e4m3_encode(double x)
 {
     uint8_t sign;
     double a, d_lo, d_hi;
     int lo, hi;
+    pthread_once(&g_grid_once, fill_grid);
     if (isnan(x))
         return 0x7F;
     sign = signbit(x) ? 0x80 : 0x00;
@@ -94,13 +106,13 @@ uint8_t orc_e4m3_encode(double x)
     hi = 0x7E;
     while (hi - lo > 1) {
         int mid = (lo + hi) / 2;
-        if (orc_e4m3_decode((uint8_t)mid) <= a)
+        if (g_grid[mid] <= a)
             lo = mid;
         else
             hi = mid;
     }
-    d_lo = a - orc_e4m3_decode((uint8_t)lo);
-    d_hi = orc_e4m3_decode((uint8_t)hi) - a;
+    d_lo = a - g_grid[lo];
+    d_hi = g_grid[hi] - a;
     if (d_lo < d_hi)
         return (uint8_t)(sign | lo);
     if (d_hi < d_lo)
