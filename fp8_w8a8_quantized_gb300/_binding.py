@@ -96,6 +96,8 @@ def lib() -> ctypes.CDLL:
         L.fp8_status_string.argtypes = [_st]
         L.fp8_device_status.restype = _st
         L.fp8_device_status.argtypes = [ctypes.c_int]
+        L.fp8_selftest_wait_timeout.restype = _st
+        L.fp8_selftest_wait_timeout.argtypes = [_i64, _vp, _vp]
         _lib = L
         return L
 

@@ -166,6 +166,19 @@ int64_t blocks_of(int64_t n) { return (n + kScaleBlock - 1) / kScaleBlock; }
 
 namespace fp8k {
 
+fp8_status_t linear_checks(const void* x, const uint8_t* wq, const float* s_w, const void* y,
+                           int64_t M, int64_t N, int64_t K) {
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return FP8_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return FP8_OK;
+    if (!x || !wq || !s_w || !y) return FP8_ERR_INVALID_ARG;
+    if (K % 16 != 0) return FP8_ERR_UNSUPPORTED;
+    if (!aligned(x, 16) || !aligned(wq, 16) || !aligned(y, 16) || !aligned(s_w, 4))
+        return FP8_ERR_UNSUPPORTED;
+    DeviceState* d = nullptr;
+    return current_device(&d);
+}
+
 bool encode_tmap_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint64_t ld_bytes, uint32_t box_cols, uint32_t box_rows) {
     EncodeTiledFn fn = encode_fn();
@@ -433,6 +446,18 @@ const char* fp8_status_string(fp8_status_t status) {
         case FP8_ERR_TIMEOUT: return "FP8_ERR_TIMEOUT";
     }
     return "FP8_ERR_UNKNOWN";
+}
+
+fp8_status_t fp8_selftest_wait_timeout(int64_t limit_ns, uint64_t* report, void* stream) {
+    if (limit_ns < 1000 || limit_ns > 100000000 || !report) return FP8_ERR_INVALID_ARG;
+    if (!aligned(report, 8)) return FP8_ERR_UNSUPPORTED;
+    DeviceState* d = nullptr;
+    fp8_status_t st = current_device(&d);
+    if (st != FP8_OK) return st;
+    cudaError_t e = fp8k::launch_wait_timeout_selftest(
+        static_cast<uint64_t>(limit_ns), d->status,
+        reinterpret_cast<unsigned long long*>(report), static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
 fp8_status_t fp8_device_status(int clear) {

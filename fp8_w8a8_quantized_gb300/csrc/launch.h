@@ -7,6 +7,8 @@
 
 #include <cstdint>
 
+#include "fp8w8a8.h"
+
 namespace fp8k {
 
 // Per-row dynamic E4M3 quantization (quant.cu).  R > 0, K % 16 == 0.
@@ -87,6 +89,17 @@ cudaError_t launch_quant_weight_blocks(const void* w, int64_t N, int64_t K, int6
 // Block-scaled GEMM (gemm_blockwise.cu): GemmArgs with s_tok = s_x
 // [M, ceil(K/128)] and s_w [ceil(N/128), ceil(K/128)].
 cudaError_t launch_gemm_blockwise(const GemmArgs& a);
+
+// Self-test of the bounded waits (selftest.cu): one CTA whose waits run out
+// after limit_ns; report[0..3] as fp8_selftest_wait_timeout documents.
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, unsigned* status,
+                                         unsigned long long* report, cudaStream_t st);
+
+// The checks fp8_linear makes on everything but its workspace (sizes,
+// pointers, alignment), then the device check (api.cu).  FP8_OK for an
+// empty layer too.
+fp8_status_t linear_checks(const void* x, const uint8_t* wq, const float* s_w, const void* y,
+                           int64_t M, int64_t N, int64_t K);
 
 // One-time per-device kernel attribute setup (dynamic shared memory limits).
 cudaError_t prepare_gemm_prefill();

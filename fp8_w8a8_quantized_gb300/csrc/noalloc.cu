@@ -24,6 +24,7 @@
 #include <mutex>
 
 #include "fp8w8a8.h"
+#include "launch.h"
 
 namespace {
 
@@ -43,8 +44,10 @@ fp8_status_t scratch_on_current_device(void** out) {
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
     if (!g_scratch_ptr[dev]) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p)
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) {
+            (void)cudaGetLastError();  // leave no pending error behind
             return FP8_ERR_CUDA;
+        }
         g_scratch_ptr[dev] = p;
     }
     *out = g_scratch_ptr[dev];
@@ -56,13 +59,16 @@ fp8_status_t scratch_on_current_device(void** out) {
 extern "C" fp8_status_t fp8_linear_static_scratch(const void* x_bf16, const uint8_t* wq,
                                                   const float* s_w, void* y_bf16, int64_t M,
                                                   int64_t N, int64_t K, void* stream) {
-    if (M < 0 || N < 0 || K < 0) return FP8_ERR_INVALID_ARG;
-    if (M == 0 || N == 0) return FP8_OK;
+    // The same argument and device checks as fp8_linear, before anything
+    // touches the array: a device the library does not support answers
+    // FP8_ERR_UNSUPPORTED here, as it would from fp8_linear.
+    fp8_status_t st = fp8k::linear_checks(x_bf16, wq, s_w, y_bf16, M, N, K);
+    if (st != FP8_OK || M == 0 || N == 0) return st;
     const size_t need = fp8_linear_workspace_size(M, N, K);
     if (need == 0) return FP8_ERR_INVALID_ARG;
     if (need > static_cast<size_t>(FP8_STATIC_SCRATCH_BYTES)) return FP8_ERR_WORKSPACE;
     void* scratch = nullptr;
-    fp8_status_t st = scratch_on_current_device(&scratch);
+    st = scratch_on_current_device(&scratch);
     if (st != FP8_OK) return st;
     return fp8_linear(x_bf16, wq, s_w, y_bf16, M, N, K, scratch, FP8_STATIC_SCRATCH_BYTES,
                       stream);

@@ -63,17 +63,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Gives up when the
-// CTA-wide abort flag is set by another role, or after kWaitLimitNs, in which
-// case it sets the abort flag and the device status word.  Returns false when
-// it gave up.
+// CTA-wide abort flag is set by another role, or after limit_ns (kWaitLimitNs
+// in every kernel but the wait self-test), in which case it sets the abort
+// flag and the device status word.  Returns false when it gave up.
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
-                                             volatile int* abort_flag, unsigned* status) {
+                                             volatile int* abort_flag, unsigned* status,
+                                             uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if ((it & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+        if ((it & 63u) == 0 && globaltimer_ns() - t0 > limit_ns) {
             *abort_flag = 1;
             atomicOr(status, kErrWaitTimeout);
             return false;
@@ -84,9 +85,10 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
 // Warp-uniform bounded wait: lane 0 waits, every lane gets its verdict, so a
 // role loop run by a whole warp stays converged.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned* status) {
+                                          unsigned* status, uint64_t limit_ns = kWaitLimitNs) {
     int ok = 1;
-    if ((threadIdx.x & 31u) == 0) ok = wait_bounded(bar, parity, abort_flag, status) ? 1 : 0;
+    if ((threadIdx.x & 31u) == 0)
+        ok = wait_bounded(bar, parity, abort_flag, status, limit_ns) ? 1 : 0;
     return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
 

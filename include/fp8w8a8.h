@@ -130,8 +130,9 @@ FP8_API fp8_status_t fp8_quant_per_channel_weights(const void* w_bf16, int64_t N
  * M, N, K < 2^31.  The fp32 summation order is fixed for a given shape, so
  * repeated calls give identical bits.
  * Kernel choice: M <= 64 uses the weight-streaming split-K kernel (weights on
- * the 128-row MMA side, tokens on the narrow side), larger M the persistent
- * 128x256-tile kernel.
+ * the 128-row MMA side, tokens on the narrow side), 65 <= M <= 255 the
+ * persistent one-SM 128x256-tile kernel, M >= 256 the persistent 256x256-tile
+ * kernel that runs each MMA on a pair of SMs (cta_group::2).
  */
 FP8_API fp8_status_t fp8_scaled_gemm(const uint8_t* xq, const float* s_tok, const uint8_t* wq,
                                      const float* s_w, void* y_bf16, int64_t M, int64_t N,
@@ -349,6 +350,30 @@ FP8_API const char* fp8_status_string(fp8_status_t status);
  * the word with a synchronous copy (it waits for the device); clear != 0
  * resets it.  Returns FP8_ERR_CUDA if the copy fails. */
 FP8_API fp8_status_t fp8_device_status(int clear);
+
+/*
+ * Self-test of the bounded device waits (failure detection).  The pages have
+ * no counterpart: it exercises this library's own safeguard.  Every wait of
+ * the GEMM kernels has a time limit; when one runs out the kernel raises a
+ * CTA-wide abort flag (the CTA's other waits give up too), drains the tensor
+ * core operations it issued, frees its tensor memory, records the timeout in
+ * the device status word and returns.  This call launches one small kernel
+ * that goes through exactly that sequence on purpose: a wait on a barrier
+ * that nothing arrives on gives up after limit_ns, and a second role waiting
+ * with the kernels' own (long) limit must return on the abort flag.
+ *
+ *   limit_ns  [in]           1e3 .. 1e8 (1 us .. 100 ms), else INVALID_ARG
+ *   report    [device, out]  4 x uint64, 8-byte aligned:
+ *                            [0] 1 if the short wait gave up (expected),
+ *                            [1] 1 if the second role returned without its
+ *                                barrier completing (expected),
+ *                            [2] ns from the start of the waits until the
+ *                                first one gave up (expected >= limit_ns),
+ *                            [3] ns until the second role returned.
+ * Afterwards fp8_device_status() returns FP8_ERR_TIMEOUT until cleared with
+ * fp8_device_status(1).  Nothing faults; the context stays usable.
+ */
+FP8_API fp8_status_t fp8_selftest_wait_timeout(int64_t limit_ns, uint64_t* report, void* stream);
 
 #ifdef __cplusplus
 }

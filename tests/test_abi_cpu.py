@@ -162,3 +162,26 @@ def test_host_checks_of_the_rmsnorm_calls(L):
     assert L.fp8_linear_rmsnorm(fake, None, 1e-6, fake, fake, fake, 4, 4, 32, fake, 4096, None) == INVALID
     assert L.fp8_linear_rmsnorm(fake, fake, 1e-6, fake, fake, fake, 4, 4, 24, fake, 4096, None) == UNSUP
     assert L.fp8_linear_rmsnorm(fake, fake, 1e-6, fake, fake, fake, 0, 4, 32, None, 0, None) == 0
+
+
+def test_host_checks_of_the_selftest_and_static_scratch_calls(L):
+    import ctypes
+    INVALID, UNSUP = 1, 2
+    fake = 1 << 20
+    # wait self-test: limit_ns outside 1 us .. 100 ms, null or misaligned report
+    assert L.fp8_selftest_wait_timeout(999, fake, None) == INVALID
+    assert L.fp8_selftest_wait_timeout(100_000_001, fake, None) == INVALID
+    assert L.fp8_selftest_wait_timeout(1_000_000, None, None) == INVALID
+    assert L.fp8_selftest_wait_timeout(1_000_000, fake + 4, None) == UNSUP
+    # static-scratch layer: the same argument checks as fp8_linear, answered
+    # before the library looks at its array or at the device
+    f = L.fp8_linear_static_scratch
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 3 + [ctypes.c_void_p]
+    assert f(None, fake, fake, fake, 4, 4, 32, None) == INVALID
+    assert f(fake, fake, fake, fake, -1, 4, 32, None) == INVALID
+    assert f(fake, fake, fake, fake, 4, 4, 24, None) == UNSUP
+    assert f(fake + 8, fake, fake, fake, 4, 4, 32, None) == UNSUP
+    assert f(fake, fake, fake + 2, fake, 4, 4, 32, None) == UNSUP
+    assert f(fake, fake, fake, fake, 0, 4, 32, None) == 0
+    assert f(fake, fake, fake, fake, 4, 0, 32, None) == 0
