@@ -46,3 +46,12 @@ def sample_rows(M: int, count: int, seed: int) -> np.ndarray:
     rng = np.random.default_rng(seed)
     mid = rng.choice(np.arange(1, M - 1), size=count - 2, replace=False)
     return np.unique(np.concatenate([[0, M - 1], mid]))
+
+
+def tile_rows(M: int, seed: int, block: int = 128) -> np.ndarray:
+    """One seeded token from every `block`-row block of M (so both 128-row
+    halves of every 256-row tile are checked), plus the first and last."""
+    rng = np.random.default_rng(seed)
+    starts = np.arange(0, M, block)
+    picks = [s + int(rng.integers(0, min(block, M - s))) for s in starts]
+    return np.unique(np.concatenate([[0, M - 1], picks]))

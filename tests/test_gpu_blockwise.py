@@ -8,7 +8,7 @@ import torch
 
 import fp8_w8a8_quantized_gb300 as pkg
 from fp8_w8a8_quantized_gb300 import workloads
-from parity import bits, check_rows, host, sample_rows
+from parity import bits, check_rows, host, sample_rows, tile_rows
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -116,7 +116,9 @@ def test_gemm_decode_sizes(oracle_mod, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(65, 512, 1024), (130, 300, 1040), (256, 1024, 4096),
-                                   (1000, 768, 2048), (129, 4096, 512)])
+                                   (1000, 768, 2048), (129, 4096, 512),
+                                   # 240 and 336 tiles on 152 persistent CTAs
+                                   (640, 12288, 512), (200, 43008, 256)])
 def test_gemm_prefill_sizes(oracle_mod, M, N, K):
     _, xq, s_x, wq, s_w = make_layer(M, N, K, 70 + M, prefill=True)
     y = pkg.fp8_scaled_gemm_blockwise(xq, s_x, wq, s_w)
@@ -130,7 +132,7 @@ def test_gemm_prefill_full_size_sampled(oracle_mod, M, K, N):
     _, xq, s_x, wq, s_w = make_layer(M, N, K, 90, prefill=True)
     y = pkg.fp8_scaled_gemm_blockwise(xq, s_x, wq, s_w)
     torch.cuda.synchronize()
-    rows = sample_rows(M, 24, seed=M + N)
+    rows = tile_rows(M, seed=M + N)
     yr = oracle_mod.gemm_blockwise(host(xq[rows]), host(s_x[rows]), host(wq), host(s_w))
     check_rows(host(y[rows].float()), yr, f"blockwise prefill {M}x{K}x{N} sampled rows")
 

@@ -50,6 +50,28 @@ def test_random_codes(oracle_mod, M, N, K):
     check_rows(y, ref, f"gemm {M}x{N}x{K}")
 
 
+# Persistent kernels walking more than one output tile per CTA (or per CTA
+# pair): the second TMEM accumulator buffer, its phase flips and the tile
+# walk.  The one-SM kernel (65 <= M < 256) runs min(tiles, 152) CTAs of
+# 128 x 256 tiles; the paired-SM kernel (M >= 256) at most 76 pairs of
+# 256 x 256 tiles.  Full outputs against the oracle.
+MULTI_TILE = [
+    (200, 28672, 1024),   # one-SM: 2 x 112 = 224 tiles, up to 2 per CTA
+    (255, 49152, 256),    # one-SM: 2 x 192 = 384 tiles, up to 3 per CTA
+    (1024, 8192, 1024),   # paired: 4 x 32 = 128 tiles, up to 2 per pair
+    (1536, 8192, 256),    # paired: 6 x 32 = 192 tiles, up to 3 per pair
+    (2304, 4864, 272),    # paired: 9 x 19 = 171 tiles, ragged K
+]
+
+
+@pytest.mark.parametrize("M,N,K", MULTI_TILE)
+def test_multi_tile_persistent(oracle_mod, M, N, K):
+    qx, s_tok, qw, s_w = random_operands(M, N, K, M + 7 * N + K)
+    y = run_gemm(qx, s_tok, qw, s_w)
+    ref = oracle_mod.scaled_gemm(qx, s_tok, qw, s_w)
+    check_rows(y, ref, f"multi-tile gemm {M}x{N}x{K}")
+
+
 @pytest.mark.parametrize("M", [1, 8, 32, 64, 128, 1024])
 def test_all_positive_long_k_accumulation(oracle_mod, M):
     # all products positive and large: exposes any loss of accumulator bits

@@ -1,16 +1,17 @@
 """GPU parity of the whole W8A8 layer (fp8_linear) on every configuration:
 quantized activation bytes and scales bit-exact (read back from the
 workspace), weight codes and scales bit-exact, outputs within tolerance.
-Small shapes are compared in full; the prefill and 70B shapes on full output
-rows of sampled tokens, with the same launch configuration the benchmark
-times."""
+Small shapes and every decode batch are compared in full; the prefill
+shapes on full output rows of one token from every 128-row block (so every
+row tile of the persistent kernels is checked), with the same launch
+configuration the benchmark times."""
 import numpy as np
 import pytest
 import torch
 
 import fp8_w8a8_quantized_gb300 as pkg
 from fp8_w8a8_quantized_gb300 import workloads
-from parity import bits, check_rows, host, sample_rows
+from parity import bits, check_rows, host, sample_rows, tile_rows
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -62,7 +63,7 @@ def test_decode_8b(oracle_mod, M, name, K, N):
 def test_prefill_8b(oracle_mod, M, name, K, N):
     x = workloads.student_t_outliers(M, K, workloads.SEED_PREFILL, DEV)
     w = workloads.weights(N, K, workloads.SEED_DECODE, DEV)
-    layer(oracle_mod, x, w, rows=sample_rows(M, 24, M + N))
+    layer(oracle_mod, x, w, rows=tile_rows(M, M + N))
 
 
 @pytest.mark.parametrize("M", workloads.M_70B)
@@ -70,9 +71,10 @@ def test_prefill_8b(oracle_mod, M, name, K, N):
 def test_llama70b(oracle_mod, M, name, K, N):
     x = workloads.gaussian_outliers(M, K, workloads.SEED_70B, DEV)
     w = workloads.weights(N, K, workloads.SEED_70B, DEV)
-    rows = sample_rows(M, 8 if N * K > 2e8 else 16, M + N)
-    layer(oracle_mod, x, w, rows=rows,
-          check_weight_rows=None if N * K < 2e8 else sample_rows(N, 2048, N))
+    # every token of the decode batch; one token of every 128-row block of
+    # the prefill batch (both halves of every 256-row tile); all weight rows
+    rows = None if M <= 64 else tile_rows(M, M + N)
+    layer(oracle_mod, x, w, rows=rows)
 
 
 def test_stress_config(oracle_mod):
