@@ -132,6 +132,14 @@ __device__ __forceinline__ void push_send(const float (&v)[MT], int M, int nl, u
             st_async_v4(dst + 16u * c, v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3], bar);
 }
 
+// After a receive wait that gave up (the status word is already set): a
+// peer that has not sent yet could still write into this CTA's receive
+// buffer, so the CTA must not exit before its peers.  A cluster barrier
+// waits for every non-exited thread of the cluster (PTX ISA, barrier.cluster):
+// peers that finished have exited and are not waited for, and every other
+// peer's waits are bounded and it sends before it exits, so this completes.
+__device__ __forceinline__ void outlive_peers() { cluster_sync_all(); }
+
 // Sum the received partials of rows [lo, lo + width) (call after recv_full
 // completed); every thread of the CTA takes part.
 template <typename Out>

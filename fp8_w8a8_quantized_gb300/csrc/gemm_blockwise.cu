@@ -540,6 +540,8 @@ __global__ void __launch_bounds__(kThreads)
         // Nothing remote touches this CTA after its partials have arrived.
         if (warp_wait_cluster_noabort(&bars->recv_full, 0, 4 * kWaitLimitNs, status))
             push_reduce(recv, splits, lo, width, M, store);
+        else
+            outlive_peers();
     } else {
         tc_fence_before();
         cluster_sync_all();

@@ -282,6 +282,8 @@ __global__ void __launch_bounds__(kThreads)
         // afterwards, so it may exit without a barrier.
         if (warp_wait_cluster_noabort(&bars->recv_full, 0, 4 * kWaitLimitNs, status))
             push_reduce(recv, splits, lo, width, M, store);
+        else
+            outlive_peers();
     } else {
         // All partials of the cluster are in shared memory after this
         // barrier, and every tcgen05 operation of this CTA has completed.
