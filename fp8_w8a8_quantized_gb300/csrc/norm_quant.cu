@@ -107,7 +107,11 @@ __global__ void __launch_bounds__(G > kBlock ? G : kBlock)
     const uint4* xr = reinterpret_cast<const uint4*>(x + (live ? row : 0) * ldx);
     const uint4* gr = reinterpret_cast<const uint4*>(gamma);
 
-    uint4 v[VPT][2];
+    // x and (up to two chunks per thread; more would spill at 1024 threads)
+    // the matching gamma chunks are loaded together, so no load sits between
+    // the two reductions
+    constexpr bool kPreG = VPT <= 2;
+    uint4 v[VPT][2], gv[kPreG ? VPT : 1][2];
     float ss = 0.0f;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
@@ -115,8 +119,16 @@ __global__ void __launch_bounds__(G > kBlock ? G : kBlock)
         if (live && c < C) {
             v[i][0] = __ldg(xr + 2 * c);
             v[i][1] = __ldg(xr + 2 * c + 1);
-            ss = sumsq8(v[i][1], sumsq8(v[i][0], ss));
+            if constexpr (kPreG) {
+                gv[i][0] = __ldg(gr + 2 * c);
+                gv[i][1] = __ldg(gr + 2 * c + 1);
+            }
         }
+    }
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int64_t c = t + static_cast<int64_t>(i) * G;
+        if (live && c < C) ss = sumsq8(v[i][1], sumsq8(v[i][0], ss));
     }
     ss = group_reduce<G, B, false>(ss, red);
     const float mean = __fdiv_rn(ss, static_cast<float>(K));
@@ -127,8 +139,13 @@ __global__ void __launch_bounds__(G > kBlock ? G : kBlock)
     for (int i = 0; i < VPT; ++i) {
         const int64_t c = t + static_cast<int64_t>(i) * G;
         if (live && c < C) {
-            m = norm8(v[i][0], __ldg(gr + 2 * c), inv, m);
-            m = norm8(v[i][1], __ldg(gr + 2 * c + 1), inv, m);
+            if constexpr (kPreG) {
+                m = norm8(v[i][0], gv[i][0], inv, m);
+                m = norm8(v[i][1], gv[i][1], inv, m);
+            } else {
+                m = norm8(v[i][0], __ldg(gr + 2 * c), inv, m);
+                m = norm8(v[i][1], __ldg(gr + 2 * c + 1), inv, m);
+            }
         }
     }
     m = group_reduce<G, B, true>(m, red);

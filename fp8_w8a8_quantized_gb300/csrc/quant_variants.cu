@@ -10,8 +10,12 @@
 //     "Turning it on in an engine").
 // The arithmetic is that of the per-token quantizer (quant_math.cuh).  All
 // are grid-stride loops over 16-element chunks (one 32-byte load, one 16-byte
-// store), memory-bound; the per-tensor amax is two launches (per-CTA maxima,
-// then every CTA reduces them), which needs no atomics and no zeroed memory.
+// store), memory-bound; contiguous tensors take a flat loop with no row
+// arithmetic and two chunks in flight per thread.  The per-tensor amax is two
+// launches (per-CTA maxima, then every CTA reduces them), which needs no
+// atomics and no zeroed memory; the first pass reads x with an L2
+// evict-last hint and the second reads it back from the end, so that much of
+// it comes from L2.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -34,15 +38,82 @@ __device__ __forceinline__ uint4 quant16(const uint4* src, const Divisor& d) {
     return make_uint4(qa.x, qa.y, qb.x, qb.y);
 }
 
+template <bool kBounded = false>
+__device__ __forceinline__ uint4 quant16v(const uint4& a, const uint4& b, const Divisor& d) {
+    const uint2 qa = quant8<kBounded>(a, d), qb = quant8<kBounded>(b, d);
+    return make_uint4(qa.x, qa.y, qb.x, qb.y);
+}
+
+// 16-byte load that does not allocate in L1, with an L2 eviction-priority
+// hint (a createpolicy result), and the matching store.
+__device__ __forceinline__ uint4 ld_hint(const uint4* p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+
+__device__ __forceinline__ void st_hint(uint4* p, const uint4& v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+}
+
+constexpr int kUnroll = 2;  // chunks in flight per thread and loop trip
+
+// Contiguous x [R, K] / s -> contiguous q: chunk i is the 16 elements at
+// offset 16 i of both, so the grid-stride loop needs no row arithmetic and
+// keeps kUnroll chunks of loads in flight per thread.  `reverse` walks the
+// chunks from the end (the per-tensor second pass: the chunks the first pass
+// read last are the likeliest still in L2; measured faster than each thread
+// revisiting its own chunks backwards).
+template <bool kBounded>
+__device__ __forceinline__ void quant_flat(const uint16_t* __restrict__ x, uint8_t* __restrict__ q,
+                                           int64_t total, const Divisor& dv, uint64_t ld_pol,
+                                           uint64_t st_pol, bool reverse) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    int64_t j = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    for (; j + (kUnroll - 1) * stride < total; j += kUnroll * stride) {
+        uint4 a[kUnroll], b[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t ch = j + u * stride;
+            const int64_t i = reverse ? total - 1 - ch : ch;
+            const uint4* src = reinterpret_cast<const uint4*>(x + i * 16);
+            a[u] = ld_hint(src, ld_pol);
+            b[u] = ld_hint(src + 1, ld_pol);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t ch = j + u * stride;
+            const int64_t i = reverse ? total - 1 - ch : ch;
+            st_hint(reinterpret_cast<uint4*>(q + i * 16), quant16v<kBounded>(a[u], b[u], dv),
+                    st_pol);
+        }
+    }
+    for (; j < total; j += stride) {
+        const int64_t i = reverse ? total - 1 - j : j;
+        const uint4* src = reinterpret_cast<const uint4*>(x + i * 16);
+        const uint4 a = ld_hint(src, ld_pol), b = ld_hint(src + 1, ld_pol);
+        st_hint(reinterpret_cast<uint4*>(q + i * 16), quant16v<kBounded>(a, b, dv), st_pol);
+    }
+}
+
 // x [R, K] (ld ldx elements) / s -> q [R, K] (ld ldq bytes), grid-stride
 // over 16-element chunks.  kBounded: s = amax / 448 of x itself.
 template <bool kBounded = false>
 __device__ __forceinline__ void quant_chunks(const uint16_t* __restrict__ x, int64_t R, int64_t K,
                                              int64_t ldx, float s, uint8_t* __restrict__ q,
-                                             int64_t ldq) {
+                                             int64_t ldq, uint64_t ld_pol, uint64_t st_pol,
+                                             bool reverse = false) {
     const int64_t C = K >> 4;
     const int64_t total = R * C;
     const Divisor dv = divisor_of(s);
+    if (ldx == K && ldq == K) {
+        quant_flat<kBounded>(x, q, total, dv, ld_pol, st_pol, reverse);
+        return;
+    }
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * kThreads) {
         const int64_t r = i / C, c = i - r * C;
@@ -66,7 +137,8 @@ __global__ void __launch_bounds__(kThreads)
     pdl_launch_dependents();
     pdl_wait_primary();
     const float s = __ldg(s_ptr);
-    quant_chunks(x, R, K, ldx, s, q, ldq);
+    const uint64_t pol = policy_evict_first();
+    quant_chunks(x, R, K, ldx, s, q, ldq, pol, pol);
     if (s_rows) fill_rows(s_rows, R, s);
 }
 
@@ -92,11 +164,35 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t C = K >> 4;
     const int64_t total = R * C;
     float m = 0.0f;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * kThreads) {
-        const int64_t r = i / C, c = i - r * C;
-        const uint4* src = reinterpret_cast<const uint4*>(x + r * ldx + c * 16);
-        m = amax8(__ldg(src + 1), amax8(__ldg(src), m));
+    if (ldx == K) {
+        // contiguous: flat chunks, four in flight per thread; the lines stay
+        // in L2 (evict_last) for the second pass
+        const uint64_t pol = policy_evict_last();
+        const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+        int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+        constexpr int U = 4;
+        for (; i + (U - 1) * stride < total; i += U * stride) {
+            uint4 a[U], b[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint4* src = reinterpret_cast<const uint4*>(x + (i + u * stride) * 16);
+                a[u] = ld_hint(src, pol);
+                b[u] = ld_hint(src + 1, pol);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) m = amax8(b[u], amax8(a[u], m));
+        }
+        for (; i < total; i += stride) {
+            const uint4* src = reinterpret_cast<const uint4*>(x + i * 16);
+            m = amax8(ld_hint(src + 1, pol), amax8(ld_hint(src, pol), m));
+        }
+    } else {
+        for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < total;
+             i += static_cast<int64_t>(gridDim.x) * kThreads) {
+            const int64_t r = i / C, c = i - r * C;
+            const uint4* src = reinterpret_cast<const uint4*>(x + r * ldx + c * 16);
+            m = amax8(__ldg(src + 1), amax8(__ldg(src), m));
+        }
     }
     m = block_max(m, red);
     if (threadIdx.x == 0) partial[blockIdx.x] = m;
@@ -115,7 +211,10 @@ __global__ void __launch_bounds__(kThreads)
     for (int i = threadIdx.x; i < n_partial; i += kThreads) m = fmaxf(m, partial[i]);
     const float s = scale_of(block_max(m, red));
     if (blockIdx.x == 0 && threadIdx.x == 0) *s_out = s;
-    quant_chunks<true>(x, R, K, ldx, s, q, ldq);
+    // last use of x: read it back from the end (the lines the first pass
+    // touched last first), evict-first, and write the codes evict-first
+    const uint64_t pol = policy_evict_first();
+    quant_chunks<true>(x, R, K, ldx, s, q, ldq, pol, pol, true);
     if (s_rows) fill_rows(s_rows, R, s);
 }
 
