@@ -47,17 +47,30 @@ _i64 = ctypes.c_int64
 _vp = ctypes.c_void_p
 
 
+# Compiler command for the oracle source (also used by the mutation test,
+# which compiles copies of it with one planted mistake each).
+CC_FLAGS = ["-O2", "-std=c11", "-fopenmp", "-pthread", "-ffp-contract=off",
+            "-fno-fast-math", "-fPIC", "-shared"]
+
+
+def compile_source(src: str, out: str) -> None:
+    subprocess.run(["gcc"] + CC_FLAGS + ["-o", out, src, "-lm"], check=True)
+
+
 def build(force: bool = False) -> str:
     """Compile the C oracle with gcc (OpenMP, IEEE fp32 division, no FMA
-    contraction).  Returns the path of the shared library."""
+    contraction).  Returns the path of the shared library.  The environment
+    variable FP8_ORACLE_LIB names another compiled copy to load instead (the
+    mutation test's planted-mistake builds)."""
+    alt = os.environ.get("FP8_ORACLE_LIB")
+    if alt:
+        return alt
     os.makedirs(_OUT_DIR, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-pthread", "-ffp-contract=off",
-           "-fno-fast-math", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
-    subprocess.run(cmd, check=True)
+    compile_source(_SRC, tmp)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
