@@ -813,7 +813,7 @@ def run_case(spec: str, reps: int = 4):
     build.build()
     dev = torch.device("cuda", 0)
     kind, *dims = spec.split(",")
-    if kind in ("static", "tensor", "kv"):
+    if kind in ("static", "tensor", "kv", "norm"):
         return run_variant_case(pkg, workloads, dev, kind, [int(v) for v in dims], reps)
     if kind == "block":
         M, K, N = (int(v) for v in dims)
@@ -851,9 +851,17 @@ def run_case(spec: str, reps: int = 4):
 
 
 def run_variant_case(pkg, workloads, dev, kind, dims, reps):
-    """static,M,K / tensor,M,K / kv,T,H,D: one quantizer variant `reps` times."""
+    """static,M,K / tensor,M,K / norm,M,K / kv,T,H,D: one quantizer variant
+    `reps` times."""
     import torch
-    if kind == "kv":
+    if kind == "norm":
+        M, K = dims
+        x = workloads.student_t_outliers(M, K, workloads.SEED_PREFILL, dev)
+        gam = (1.0 + 0.1 * torch.randn(K, device=dev)).to(torch.bfloat16)
+        q = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        s_rows = torch.empty(M, dtype=torch.float32, device=dev)
+        run = lambda: pkg.fp8_rmsnorm_quant(x, gam, 1e-6, xq=q, s_tok=s_rows)
+    elif kind == "kv":
         T, H, D = dims
         kv = workloads.student_t_outliers(T * H, D, workloads.SEED_PREFILL, dev).view(T, H, D)
         cache = torch.zeros((T + 1024, H, D), dtype=torch.uint8, device=dev)
@@ -889,7 +897,8 @@ def main():
                     help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--case", default=None,
                     help="M,K,N: run fp8_linear on that one layer a few times and exit; "
-                         "static,M,K / tensor,M,K / kv,T,H,D: one quantizer variant; "
+                         "static,M,K / tensor,M,K / norm,M,K / kv,T,H,D: one quantizer "
+                         "variant; "
                          "block,M,K,N: fp8_linear_blockwise on one layer")
     args = ap.parse_args()
     if args.case:
