@@ -14,10 +14,12 @@
 //
 // Same work layout as quant.cu (G threads per row, VPT 16-element chunks per
 // thread held in registers; x is read once).  The sum of squares is each
-// thread's chunks in order, then a butterfly over the warp, then the warps'
-// partial sums in order: at most 16 VPT - 1 + 5 + 31 < 128 roundings of
-// non-negative terms, so the fp32 sum is within 128 * 2^-24 = 2^-17 of the
-// exact one (relative); every later step is an IEEE operation.
+// thread's chunks in order into two running sums (even and odd elements,
+// one packed FMA per pair) added at the end, then a butterfly over the warp,
+// then the warps' partial sums in order: at most 8 VPT + 1 + 5 + 31 < 128
+// roundings of non-negative terms on any path, so the fp32 sum is within
+// 128 * 2^-24 = 2^-17 of the exact one (relative); every later step is an
+// IEEE operation.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -55,17 +57,25 @@ __device__ __forceinline__ float group_reduce(float v, float* red) {
     return v;
 }
 
-__device__ __forceinline__ float sumsq2(uint32_t w, float s) {
+// Sum of squares of a bf16 pair into two running sums (the low and the
+// high lanes), one packed f32x2 FMA; a * a is exact for a bf16 value.
+__device__ __forceinline__ void sumsq2(uint32_t w, float& s0, float& s1) {
     const float a = bf16lo(w), b = bf16hi(w);
-    return fmaf(b, b, fmaf(a, a, s));  // a * a is exact for a bf16 value
+    fma2(s0, s1, a, b, a, b);
 }
 
-__device__ __forceinline__ float sumsq8(const uint4& v, float s) {
-    return sumsq2(v.w, sumsq2(v.z, sumsq2(v.y, sumsq2(v.x, s))));
+__device__ __forceinline__ void sumsq8(const uint4& v, float& s0, float& s1) {
+    sumsq2(v.x, s0, s1);
+    sumsq2(v.y, s0, s1);
+    sumsq2(v.z, s0, s1);
+    sumsq2(v.w, s0, s1);
 }
 
-__device__ __forceinline__ uint16_t bf16_bits(float f) {
-    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+// Two fp32 values -> a bf16 pair (round to nearest even), `lo` in the low half.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 // One bf16 pair normalised (x * inv * g, each product rounded to fp32, then
@@ -77,7 +87,7 @@ __device__ __forceinline__ uint32_t norm2(uint32_t xw, uint32_t gw, float inv) {
     fma2(lo, hi, bf16lo(xw), bf16hi(xw), inv, inv);
     float ylo = -0.0f, yhi = -0.0f;
     fma2(ylo, yhi, lo, hi, bf16lo(gw), bf16hi(gw));
-    return static_cast<uint32_t>(bf16_bits(ylo)) | (static_cast<uint32_t>(bf16_bits(yhi)) << 16);
+    return bf16x2_rn(ylo, yhi);
 }
 
 // Normalise 8 values in place; returns the running max |y|.
@@ -125,11 +135,16 @@ __global__ void __launch_bounds__(G > kBlock ? G : kBlock)
             }
         }
     }
+    float s1 = 0.0f;  // ss collects the low lanes, s1 the high lanes
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         const int64_t c = t + static_cast<int64_t>(i) * G;
-        if (live && c < C) ss = sumsq8(v[i][1], sumsq8(v[i][0], ss));
+        if (live && c < C) {
+            sumsq8(v[i][0], ss, s1);
+            sumsq8(v[i][1], ss, s1);
+        }
     }
+    ss = __fadd_rn(ss, s1);
     ss = group_reduce<G, B, false>(ss, red);
     const float mean = __fdiv_rn(ss, static_cast<float>(K));
     const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
