@@ -753,7 +753,8 @@ def variant_rates(pkg, workloads, dev, stream, timed, hbm_peak, steps):
                                                  s_rows=s_rows, workspace=ws, stream=stream),
               n, 3)
     out["per_tensor"] = dict(rate(t, act_bytes), workload=f"{M}x{K} bf16", launches=2,
-                             note="two passes over x; the second mostly hits L2")
+                             note="two passes over x; the second reads it back from the end, "
+                                  "partly from L2")
     # RMSNorm with the quantizer fused in, against RMSNorm written to bf16
     # (torch, a library kernel: context only) followed by the quantizer
     gam = (1.0 + 0.1 * torch.randn(K, device=dev)).to(torch.bfloat16)
