@@ -229,16 +229,35 @@ __global__ void __launch_bounds__(kThreads)
     pdl_wait_primary();
     const int64_t C = D >> 4;  // chunks per head
     const int64_t total = T * H * C;
+    const uint32_t C32 = static_cast<uint32_t>(C), H32 = static_cast<uint32_t>(H);
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * kThreads) {
-        const int64_t th = i / C, c = i - th * C;
-        const int64_t t = th / H, h = th - t * H;
+        // x is contiguous [T, H, D]: chunk i starts at element 16 i.  The
+        // source is loaded before the slot is known (the slot only decides
+        // where, or whether, the codes go), and the index arithmetic is
+        // 32-bit whenever the chunk count allows.
+        const uint4* src = reinterpret_cast<const uint4*>(x + i * 16);
+        const uint4 a = __ldg(src), b = __ldg(src + 1);
+        uint32_t c, h;
+        int64_t t;
+        if (total <= 0xFFFFFFFFll) {
+            const uint32_t i32 = static_cast<uint32_t>(i);
+            const uint32_t th = i32 / C32;  // token * H + head
+            c = i32 - th * C32;
+            const uint32_t t32 = th / H32;
+            h = th - t32 * H32;
+            t = t32;
+        } else {
+            const int64_t th = i / C;
+            c = static_cast<uint32_t>(i - th * C);
+            t = th / H;
+            h = static_cast<uint32_t>(th - t * H);
+        }
         const int64_t row = slot ? __ldg(slot + t) : t;
         if (row < 0 || row >= n_slots) continue;
         const float s = __ldg(scale + h * scale_stride);
-        const uint4* src = reinterpret_cast<const uint4*>(x + th * D + c * 16);
         *reinterpret_cast<uint4*>(cache + (row * H + h) * D + c * 16) =
-            quant16(src, divisor_of(s));
+            quant16v(a, b, divisor_of(s));
     }
 }
 
