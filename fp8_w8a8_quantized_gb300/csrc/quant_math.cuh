@@ -55,7 +55,7 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
 // scale whose reciprocal is not a normal number (s below the normal range or
 // above 2^126), or that is not finite, takes the IEEE division.
 struct Divisor {
-    float s, ns, r;  // s, -s, RN(1/s)
+    float s, ns, r, nr;  // s, -s, RN(1/s), -RN(1/s)
     bool ieee;
 };
 
@@ -64,6 +64,7 @@ __device__ __forceinline__ Divisor divisor_of(float s) {
     d.s = s;
     d.ns = -s;
     d.r = __frcp_rn(s);
+    d.nr = -d.r;
     d.ieee = !(s >= 1.17549435e-38f && s <= 8.50705917e37f);  // [2^-126, 2^126]
     return d;
 }
@@ -79,22 +80,29 @@ __device__ __forceinline__ float div_rn(float x, const Divisor& d) {
 
 // One bf16 pair -> two codes in the low 16 bits: div_rn on both values in
 // packed f32x2 fused multiply-adds (each lane an IEEE fp32 FMA, so the same
-// bits).  q0 = RN(x * r) is formed as RN(x * r + (-0)), which equals the
-// product's rounding for every x, signed zeros included.  kBounded: the
-// scale comes from these values' own maximum (s = amax / 448), so |q0| stays
-// near 448 and cannot overflow; otherwise an infinite q0 is kept, as in
-// div_rn.
+// bits).  The pair is unpacked negated, z = -x (one integer multiply-add and
+// one logic op: z_lo = (u << 16) + 2^31, z_hi = (u & 0xffff0000) ^ 2^31), and
+// the steps run on z with -r:
+//   q0 = RN(z * (-r) + (-0))  = RN(x * r)       (the same product)
+//   e' = RN(q0 * s + z)       = -(x - s * q0)   (exact)
+//   y  = RN(e' * (-r) + q0)   = RN(q0 + e * r)  (the same fused sum)
+// so every nonzero result has the bits of div_rn.  The sign of a zero
+// result comes out right without a copysign: x = -0 gives q0 = -0,
+// e' = +0 and y = (+0)(-r) + (-0) = -0; x = +0 gives +0; a nonzero x whose
+// quotient underflows gives RN(x * r) = zero with the sign of x.  kBounded:
+// the scale comes from these values' own maximum (s = amax / 448), so |q0|
+// stays near 448 and cannot overflow; otherwise an infinite q0 is kept, as
+// in div_rn.
 template <bool kBounded>
 __device__ __forceinline__ uint32_t quant2(uint32_t u, const Divisor& d) {
-    const float x0 = bf16lo(u), x1 = bf16hi(u);
+    const float z0 = __uint_as_float(u * 0x10000u + 0x80000000u);
+    const float z1 = __uint_as_float((u & 0xFFFF0000u) ^ 0x80000000u);
     float q0 = -0.0f, q1 = -0.0f;
-    fma2(q0, q1, x0, x1, d.r, d.r);
-    float e0 = x0, e1 = x1;
-    fma2(e0, e1, q0, q1, d.ns, d.ns);  // x - s * q0, exact
+    fma2(q0, q1, z0, z1, d.nr, d.nr);
+    float e0 = z0, e1 = z1;
+    fma2(e0, e1, q0, q1, d.s, d.s);  // s * q0 - x, exact
     float y0 = q0, y1 = q1;
-    fma2(y0, y1, e0, e1, d.r, d.r);
-    y0 = copysignf(y0, x0);
-    y1 = copysignf(y1, x1);
+    fma2(y0, y1, e0, e1, d.nr, d.nr);
     if (!kBounded) {
         y0 = isinf(q0) ? q0 : y0;
         y1 = isinf(q1) ? q1 : y1;
