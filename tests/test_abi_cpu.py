@@ -185,3 +185,19 @@ def test_host_checks_of_the_selftest_and_static_scratch_calls(L):
     assert f(fake, fake, fake + 2, fake, 4, 4, 32, None) == UNSUP
     assert f(fake, fake, fake, fake, 0, 4, 32, None) == 0
     assert f(fake, fake, fake, fake, 4, 0, 32, None) == 0
+
+
+def test_calls_that_pass_the_checks_report_a_cuda_error_without_a_device(L):
+    """With no usable GPU the first CUDA call fails, and a call that passed
+    every host check answers FP8_ERR_CUDA (nothing is launched).  Skipped
+    where a GPU is present: there these fake pointers would reach a kernel."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this case needs a machine without one")
+    CUDA = 4
+    fake = 1 << 20
+    assert L.fp8_quant_per_token(fake, 4, 32, 32, fake, 32, fake, None) == CUDA
+    assert L.fp8_scaled_gemm(fake, fake, fake, fake, fake, 4, 4, 32, None, 0, None) == CUDA
+    assert L.fp8_linear(fake, fake, fake, fake, 4, 4, 32, fake, 4096, None) == CUDA
+    assert L.fp8_device_status(0) == CUDA
+    assert L.fp8_selftest_wait_timeout(1_000_000, fake, None) == CUDA
