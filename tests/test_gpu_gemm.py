@@ -143,3 +143,48 @@ def test_empty_and_rejected_calls():
                              y.data_ptr() + 2, 4, 4, 64, None, 0, s) == 2
     torch.cuda.synchronize()
     assert torch.all(y == 0)
+
+
+# Codes whose values lie in [1, 2) (E4M3 exponent field 7, either sign):
+# every product is a multiple of 2^-6 below 4, so for K <= 2048 every partial
+# sum is exactly representable in fp32, whatever order and split the kernel
+# adds in.  The GPU's fp32 accumulator then equals the oracle's exact sum, and
+# the output must equal bf16_rn(fl32(fl32(acc * s_tok[m]) * s_w[n])) bit for
+# bit: this pins the epilogue (its multiplication order and the round to
+# nearest even into bf16) on all three GEMM kernels, beyond the tolerance.
+# Codes whose values make every fp32 partial sum exact, in any order and any
+# split of K: +-1 alone (integer sums, at most K), and all codes with values
+# in [1, 2) (products are multiples of 2^-6 below 4, so sums of up to 2048 of
+# them need at most 19 significant bits).  With the accumulator fixed, the
+# epilogue's fp32 products and bf16 rounding are compared bit for bit.
+EXACT_CODE_SETS = {
+    "unit": np.array([0x38, 0xB8], dtype=np.uint8),
+    "one_to_two": np.array([c | s for c in range(0x38, 0x40) for s in (0x00, 0x80)],
+                           dtype=np.uint8),
+}
+
+
+@pytest.mark.parametrize("codes", sorted(EXACT_CODE_SETS))
+@pytest.mark.parametrize("M,N,K", [(1, 256, 1024), (8, 520, 512), (32, 384, 2048),
+                                   (64, 1000, 1040), (100, 300, 1024), (200, 28672, 256),
+                                   (300, 520, 1024), (1024, 8192, 512)])
+def test_epilogue_bits_with_exact_sums(oracle_mod, codes, M, N, K):
+    rng = np.random.default_rng(M * 7 + N + K)
+    qx = rng.choice(EXACT_CODE_SETS[codes], size=(M, K))
+    qw = rng.choice(EXACT_CODE_SETS[codes], size=(N, K))
+    s_tok = np.exp2(rng.uniform(-12, 4, M)).astype(np.float32)
+    s_w = np.exp2(rng.uniform(-12, 0, N)).astype(np.float32)
+    y = pkg.fp8_scaled_gemm(dev(qx), dev(s_tok), dev(qw), dev(s_w))
+    torch.cuda.synchronize()
+    assert pkg.fp8_device_status() == 0
+    acc = oracle_mod.gemm_exact(qx, qw)                       # exact, scaled by 2^18
+    acc32 = (acc.astype(np.float64) * 2.0 ** -18).astype(np.float32)
+    assert np.array_equal(acc32.astype(np.float64) * 2.0 ** 18, acc.astype(np.float64))
+    t = (acc32 * s_tok[:, None]) * s_w[None, :]              # fp32 products, in order
+    expect = torch.from_numpy(t.astype(np.float32)).to(torch.bfloat16).float()
+    got = y.cpu().float()                                     # exact widening
+    # value equality: bitwise except that +0 and -0 of a zero sum are equal
+    diff = (got != expect).nonzero()
+    assert diff.numel() == 0, (
+        f"{codes} {M}x{N}x{K}: {diff.shape[0]} outputs differ, first at {diff[0].tolist()}: "
+        f"got {got[tuple(diff[0])].item()!r}, expected {expect[tuple(diff[0])].item()!r}")
