@@ -108,6 +108,74 @@ def test_per_tensor_is_deterministic():
     assert torch.equal(q1, q2) and torch.equal(s1, s2)
 
 
+def test_per_tensor_strided_rows(oracle_mod):
+    # rows with a stride (the row-wise loops of both passes)
+    M, K, ldx, ldq = 301, 1024, 1040, 1056
+    base = workloads.gaussian_outliers(M, ldx, 13, DEV)
+    x = base[:, :K]
+    xq = torch.full((M, ldq), 0xAB, dtype=torch.uint8, device=DEV)
+    s = torch.empty(1, dtype=torch.float32, device=DEV)
+    ws = torch.empty(int(pkg.lib().fp8_quant_per_tensor_workspace_size(M, K)), dtype=torch.uint8,
+                     device=DEV)
+    st = pkg.lib().fp8_quant_per_tensor(x.data_ptr(), M, K, ldx, xq.data_ptr(), ldq, s.data_ptr(),
+                                        None, ws.data_ptr(), ws.numel(),
+                                        torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert pkg.fp8_device_status() == 0
+    q_ref, s_ref = oracle_mod.quant_tensor_bf16(bits(x))
+    assert host(s)[0].view(np.uint32) == np.float32(s_ref).view(np.uint32)
+    assert_codes(xq[:, :K], q_ref, "per-tensor strided")
+    assert np.all(host(xq)[:, K:] == 0xAB), "wrote past K"
+
+
+@pytest.mark.parametrize("where", ["first", "middle", "last"])
+def test_per_tensor_maximum_anywhere_in_a_large_tensor(oracle_mod, where):
+    # 64 MB of activations (the grid-stride passes wrap many times); the
+    # maximum is planted at the first value (the first chunk of the first
+    # CTA), in the middle, or at the very last value (the last chunk, read
+    # first by the second pass)
+    M, K = 8192, 4096
+    x = randn((M, K), 31, 1.0)
+    r, c = {"first": (0, 0), "middle": (M // 2 + 5, K // 3 + 1), "last": (M - 1, K - 1)}[where]
+    x[r, c] = -3072.0
+    s_rows = torch.empty(M, dtype=torch.float32, device=DEV)
+    q, s = pkg.fp8_quant_per_tensor(x, s_rows=s_rows)
+    torch.cuda.synchronize()
+    assert pkg.fp8_device_status() == 0
+    assert host(s)[0] == np.float32(3072.0) / np.float32(448.0)
+    assert np.all(host(s_rows) == host(s)[0])
+    q_ref, s_ref = oracle_mod.quant_tensor_bf16(bits(x))
+    assert np.float32(s_ref) == host(s)[0]
+    assert_codes(q, q_ref, f"per-tensor, maximum {where}")
+
+
+def test_per_tensor_in_a_cuda_graph(oracle_mod):
+    # both launches of the per-tensor quantizer captured in a CUDA graph:
+    # replays with new contents give new, exact results (nothing is kept
+    # from one call to the next in the workspace)
+    M, K = 2048, 4096
+    x = torch.empty((M, K), dtype=torch.bfloat16, device=DEV)
+    q = torch.empty((M, K), dtype=torch.uint8, device=DEV)
+    s = torch.empty(1, dtype=torch.float32, device=DEV)
+    x.copy_(randn((M, K), 40, 1.0))
+    pkg.fp8_quant_per_tensor(x, xq=q, s=s)  # warm-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            pkg.fp8_quant_per_tensor(x, xq=q, s=s)
+    for seed, scale in [(41, 0.25), (42, 7.0), (43, 0.001)]:
+        x.copy_(randn((M, K), seed, scale))
+        g.replay()
+        torch.cuda.synchronize()
+        assert pkg.fp8_device_status() == 0
+        q_ref, s_ref = oracle_mod.quant_tensor_bf16(bits(x))
+        assert host(s)[0].view(np.uint32) == np.float32(s_ref).view(np.uint32)
+        assert_codes(q, q_ref, f"per-tensor graph replay {seed}")
+
+
 @pytest.mark.parametrize("M", [4, 32, 300])
 def test_per_tensor_codes_feed_the_scaled_gemm(oracle_mod, M):
     N, K = 512, 4096
