@@ -79,14 +79,12 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
 }
 
 // One bf16 pair normalised (x * inv * g, each product rounded to fp32, then
-// bf16).  The products are packed f32x2 fused multiply-adds with a -0
-// addend: RN(a * b + (-0)) is RN(a * b) for every a, b, signed zeros
-// included.
+// bf16), the products as packed f32x2 multiplies.
 __device__ __forceinline__ uint32_t norm2(uint32_t xw, uint32_t gw, float inv) {
-    float lo = -0.0f, hi = -0.0f;
-    fma2(lo, hi, bf16lo(xw), bf16hi(xw), inv, inv);
-    float ylo = -0.0f, yhi = -0.0f;
-    fma2(ylo, yhi, lo, hi, bf16lo(gw), bf16hi(gw));
+    float lo, hi;
+    mul2(lo, hi, bf16lo(xw), bf16hi(xw), inv, inv);
+    float ylo, yhi;
+    mul2(ylo, yhi, lo, hi, bf16lo(gw), bf16hi(gw));
     return bf16x2_rn(ylo, yhi);
 }
 
@@ -99,8 +97,12 @@ __device__ __forceinline__ float norm8(uint4& v, const uint4& g, float inv, floa
     return amax8(v, m);
 }
 
+// CTAs of kBlock threads are held to five per SM worth of registers (48 a
+// thread, no spill): the kernel is bound by issue and latency, and five
+// resident CTAs instead of the four that its natural register count allows
+// measured 7% faster (8192 x 4096).
 template <int G, int VPT>
-__global__ void __launch_bounds__(G > kBlock ? G : kBlock)
+__global__ void __launch_bounds__(G > kBlock ? G : kBlock, G > kBlock ? 1 : 5)
     rmsnorm_quant_rows(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma, float eps,
                        int64_t R, int64_t K, int64_t ldx, uint8_t* __restrict__ q, int64_t ldq,
                        float* __restrict__ s, uint16_t* __restrict__ y_out) {

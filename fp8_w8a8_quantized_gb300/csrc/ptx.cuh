@@ -347,6 +347,18 @@ __device__ __forceinline__ void fma2(float& a0, float& a1, float b0, float b1, f
         : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
+// (r0, r1) = (b0 * c0, b1 * c1): two fp32 products (round to nearest, as
+// __fmul_rn, subnormals kept) in one packed f32x2 instruction.
+__device__ __forceinline__ void mul2(float& r0, float& r1, float b0, float b1, float c0, float c1) {
+    asm("{\n\t.reg .b64 pr, pb, pc;\n\t"
+        "mov.b64 pb, {%2, %3};\n\t"
+        "mov.b64 pc, {%4, %5};\n\t"
+        "mul.rn.f32x2 pr, pb, pc;\n\t"
+        "mov.b64 {%0, %1}, pr;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA, tcgen05.mma operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -83,7 +83,7 @@ __device__ __forceinline__ float div_rn(float x, const Divisor& d) {
 // bits).  The pair is unpacked negated, z = -x (one integer multiply-add and
 // one logic op: z_lo = (u << 16) + 2^31, z_hi = (u & 0xffff0000) ^ 2^31), and
 // the steps run on z with -r:
-//   q0 = RN(z * (-r) + (-0))  = RN(x * r)       (the same product)
+//   q0 = RN(z * (-r))         = RN(x * r)       (the same product)
 //   e' = RN(q0 * s + z)       = -(x - s * q0)   (exact)
 //   y  = RN(e' * (-r) + q0)   = RN(q0 + e * r)  (the same fused sum)
 // so every nonzero result has the bits of div_rn.  The sign of a zero
@@ -97,8 +97,8 @@ template <bool kBounded>
 __device__ __forceinline__ uint32_t quant2(uint32_t u, const Divisor& d) {
     const float z0 = __uint_as_float(u * 0x10000u + 0x80000000u);
     const float z1 = __uint_as_float((u & 0xFFFF0000u) ^ 0x80000000u);
-    float q0 = -0.0f, q1 = -0.0f;
-    fma2(q0, q1, z0, z1, d.nr, d.nr);
+    float q0, q1;
+    mul2(q0, q1, z0, z1, d.nr, d.nr);
     float e0 = z0, e1 = z1;
     fma2(e0, e1, q0, q1, d.s, d.s);  // s * q0 - x, exact
     float y0 = q0, y1 = q1;
