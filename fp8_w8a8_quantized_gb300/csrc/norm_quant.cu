@@ -97,12 +97,12 @@ __device__ __forceinline__ float norm8(uint4& v, const uint4& g, float inv, floa
     return amax8(v, m);
 }
 
-// CTAs of kBlock threads are held to five per SM worth of registers (48 a
-// thread, no spill): the kernel is bound by issue and latency, and five
-// resident CTAs instead of the four that its natural register count allows
-// measured 7% faster (8192 x 4096).
+// CTAs of kBlock threads are held to six per SM worth of registers (40 a
+// thread, no spill): the kernel is bound by issue and latency, and more
+// resident warps hide more of it (8192 x 4096: 4240 GB/s at four CTAs per
+// SM, 4600 at five, 4770 at six with gamma loaded after the sum of squares).
 template <int G, int VPT>
-__global__ void __launch_bounds__(G > kBlock ? G : kBlock, G > kBlock ? 1 : 5)
+__global__ void __launch_bounds__(G > kBlock ? G : kBlock, G > kBlock ? 1 : 6)
     rmsnorm_quant_rows(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma, float eps,
                        int64_t R, int64_t K, int64_t ldx, uint8_t* __restrict__ q, int64_t ldq,
                        float* __restrict__ s, uint16_t* __restrict__ y_out) {
@@ -119,10 +119,12 @@ __global__ void __launch_bounds__(G > kBlock ? G : kBlock, G > kBlock ? 1 : 5)
     const uint4* xr = reinterpret_cast<const uint4*>(x + (live ? row : 0) * ldx);
     const uint4* gr = reinterpret_cast<const uint4*>(gamma);
 
-    // x and (up to two chunks per thread; more would spill at 1024 threads)
-    // the matching gamma chunks are loaded together, so no load sits between
-    // the two reductions
-    constexpr bool kPreG = VPT <= 2;
+    // The matching gamma chunks are loaded together with x where registers
+    // allow (one chunk per thread, or two in the large CTAs), so no load
+    // sits between the two reductions; the register-bounded two-chunk CTAs
+    // load gamma after the sum of squares instead (an L1 hit: every row
+    // reads the same gamma).
+    constexpr bool kPreG = VPT == 1 || (G > kBlock && VPT <= 2);
     uint4 v[VPT][2], gv[kPreG ? VPT : 1][2];
     float ss = 0.0f;
 #pragma unroll
