@@ -155,7 +155,9 @@ __device__ __forceinline__ float block_max(float m, float* red) {
 }
 
 // Pass 1 of the per-tensor scale: partial[b] = max |x| over this CTA's chunks.
-__global__ void __launch_bounds__(kThreads)
+// Held to 32 registers (no spill) so that all eight CTAs per SM of the grid
+// are resident: more loads in flight (measured +2% on the per-tensor pair).
+__global__ void __launch_bounds__(kThreads, 8)
     tensor_amax_partial(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx,
                         float* __restrict__ partial) {
     __shared__ float red[kThreads / 32];
