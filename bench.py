@@ -805,6 +805,13 @@ def variant_rates(pkg, workloads, dev, stream, timed, hbm_peak, steps):
     out["kv_cache_write"] = dict(rate(t, 3 * T * H * D + 8 * T),
                                  workload=f"T={T} H={H} D={D}, per-head scales, paged slots",
                                  launches=1)
+    # the same layer's keys and values in one launch (pairs of the tensors above)
+    t = graphed(lambda i: pkg.fp8_kv_cache_quant_kv(
+        kvs[2 * i % nl], kvs[(2 * i + 1) % nl], kv_scale, kv_scale, caches[2 * i % nl],
+        caches[(2 * i + 1) % nl], slots, stream=stream), nl // 2)
+    out["kv_cache_write_kv"] = dict(rate(t, 6 * T * H * D + 8 * T),
+                                    workload=f"T={T} H={H} D={D}, keys and values, per-head "
+                                             f"scales, paged slots", launches=1)
     del kvs, caches
     torch.cuda.synchronize()
     return out

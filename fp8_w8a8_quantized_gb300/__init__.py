@@ -12,6 +12,7 @@ from ._binding import (  # noqa: F401
     QuantizedLinear,
     fp8_device_status,
     fp8_kv_cache_quant,
+    fp8_kv_cache_quant_kv,
     fp8_linear,
     fp8_linear_blockwise,
     fp8_linear_blockwise_workspace_size,

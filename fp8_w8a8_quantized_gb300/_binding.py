@@ -74,6 +74,9 @@ def lib() -> ctypes.CDLL:
         L.fp8_quant_per_tensor_workspace_size.argtypes = [_i64, _i64]
         L.fp8_kv_cache_quant.restype = _st
         L.fp8_kv_cache_quant.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _i64, _vp]
+        L.fp8_kv_cache_quant_kv.restype = _st
+        L.fp8_kv_cache_quant_kv.argtypes = [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _i64, _vp, _vp,
+                                            _vp, _i64, _vp]
         L.fp8_quant_per_token_group.restype = _st
         L.fp8_quant_per_token_group.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp]
         L.fp8_quant_weight_blocks.restype = _st
@@ -243,6 +246,29 @@ def fp8_kv_cache_quant(kv: torch.Tensor, scale: torch.Tensor, cache: torch.Tenso
                                     _ptr(cache), cache.shape[0], _stream(stream)),
            "fp8_kv_cache_quant")
     return cache
+
+
+def fp8_kv_cache_quant_kv(k: torch.Tensor, v: torch.Tensor, k_scale: torch.Tensor,
+                          v_scale: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                          slot_mapping: torch.Tensor | None = None, stream=None):
+    """Keys and values of one layer in one launch: fp8_kv_cache_quant on
+    (k, k_scale, k_cache) and on (v, v_scale, v_cache) with the same slots."""
+    for t in (k, v, k_cache, v_cache):
+        if t.dim() != 3 or not t.is_contiguous():
+            raise ValueError("k, v and the caches must be contiguous [T, H, D] / [n_slots, H, D]")
+    T, H, D = k.shape
+    if v.shape != k.shape or k_cache.shape != v_cache.shape or k_cache.shape[1:] != (H, D):
+        raise ValueError("k and v must be [T, H, D], both caches [n_slots, H, D]")
+    if k_scale.numel() != v_scale.numel():
+        raise ValueError("k_scale and v_scale must have the same number of entries")
+    stride = 1 if k_scale.numel() == H and H > 1 else 0
+    if stride == 0 and k_scale.numel() != 1:
+        raise ValueError("scales must have 1 or H entries")
+    _check(lib().fp8_kv_cache_quant_kv(_ptr(k), _ptr(v), T, H, D, _ptr(k_scale), _ptr(v_scale),
+                                       stride, _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+                                       k_cache.shape[0], _stream(stream)),
+           "fp8_kv_cache_quant_kv")
+    return k_cache, v_cache
 
 
 def fp8_rmsnorm_quant(x: torch.Tensor, gamma: torch.Tensor, eps: float,

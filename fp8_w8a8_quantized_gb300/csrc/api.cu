@@ -302,26 +302,49 @@ fp8_status_t fp8_quant_per_tensor(const void* x_bf16, int64_t M, int64_t K, int6
     return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
-fp8_status_t fp8_kv_cache_quant(const void* kv_bf16, int64_t T, int64_t H, int64_t D,
-                                const float* scale, int64_t scale_stride,
-                                const int64_t* slot_mapping, uint8_t* cache, int64_t n_slots,
-                                void* stream) {
+namespace {
+// Shared by the one-tensor and the keys-and-values entry points; x1, scale1
+// and cache1 are null for the first.
+fp8_status_t kv_cache_write(const void* x0, const void* x1, int64_t T, int64_t H, int64_t D,
+                            const float* scale0, const float* scale1, int64_t scale_stride,
+                            const int64_t* slot_mapping, uint8_t* cache0, uint8_t* cache1,
+                            int64_t n_slots, bool pair, void* stream) {
     if (T < 0 || H < 0 || D < 0 || n_slots < 0 || scale_stride < 0 || T > kMaxDim ||
         H > kMaxDim || D > kMaxDim || n_slots > kMaxDim)
         return FP8_ERR_INVALID_ARG;
     if (T == 0 || H == 0 || D == 0 || n_slots == 0) return FP8_OK;
-    if (!kv_bf16 || !scale || !cache) return FP8_ERR_INVALID_ARG;
+    if (!x0 || !scale0 || !cache0 || (pair && (!x1 || !scale1 || !cache1)))
+        return FP8_ERR_INVALID_ARG;
     if (D % 16 != 0) return FP8_ERR_UNSUPPORTED;
-    if (!aligned(kv_bf16, 16) || !aligned(cache, 16) || !aligned(scale, 4) ||
+    if (!aligned(x0, 16) || !aligned(cache0, 16) || !aligned(scale0, 4) ||
+        (pair && (!aligned(x1, 16) || !aligned(cache1, 16) || !aligned(scale1, 4))) ||
         (slot_mapping && !aligned(slot_mapping, 8)))
         return FP8_ERR_UNSUPPORTED;
     DeviceState* d = nullptr;
     fp8_status_t st = current_device(&d);
     if (st != FP8_OK) return st;
-    cudaError_t e = fp8k::launch_kv_cache_quant(kv_bf16, T, H, D, scale, scale_stride,
-                                                slot_mapping, cache, n_slots, d->num_sms,
-                                                static_cast<cudaStream_t>(stream));
+    cudaError_t e = fp8k::launch_kv_cache_quant(x0, x1, T, H, D, scale0, scale1, scale_stride,
+                                                slot_mapping, cache0, cache1, n_slots,
+                                                d->num_sms, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+}  // namespace
+
+fp8_status_t fp8_kv_cache_quant(const void* kv_bf16, int64_t T, int64_t H, int64_t D,
+                                const float* scale, int64_t scale_stride,
+                                const int64_t* slot_mapping, uint8_t* cache, int64_t n_slots,
+                                void* stream) {
+    return kv_cache_write(kv_bf16, nullptr, T, H, D, scale, nullptr, scale_stride, slot_mapping,
+                          cache, nullptr, n_slots, false, stream);
+}
+
+fp8_status_t fp8_kv_cache_quant_kv(const void* k_bf16, const void* v_bf16, int64_t T, int64_t H,
+                                   int64_t D, const float* k_scale, const float* v_scale,
+                                   int64_t scale_stride, const int64_t* slot_mapping,
+                                   uint8_t* k_cache, uint8_t* v_cache, int64_t n_slots,
+                                   void* stream) {
+    return kv_cache_write(k_bf16, v_bf16, T, H, D, k_scale, v_scale, scale_stride, slot_mapping,
+                          k_cache, v_cache, n_slots, true, stream);
 }
 
 fp8_status_t fp8_quant_per_token_group(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,

@@ -66,11 +66,14 @@ constexpr int kMaxTensorPartials = 2048;
 cudaError_t launch_quant_per_tensor(const void* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q,
                                     int64_t ldq, float* s_out, float* s_rows, float* partial,
                                     int num_sms, cudaStream_t st);
-// KV-cache write: x [T, H, D] -> cache[slot[t] (or t), h, :] with scale
-// scale[h * scale_stride]; tokens whose slot is negative or >= n_slots are skipped.
-cudaError_t launch_kv_cache_quant(const void* x, int64_t T, int64_t H, int64_t D,
-                                  const float* scale, int64_t scale_stride, const int64_t* slot,
-                                  uint8_t* cache, int64_t n_slots, int num_sms, cudaStream_t st);
+// KV-cache write: x0 [T, H, D] -> cache0[slot[t] (or t), h, :] with scale
+// scale0[h * scale_stride]; tokens whose slot is negative or >= n_slots are
+// skipped.  x1 non-null: the same for x1 / scale1 / cache1 in the same launch.
+cudaError_t launch_kv_cache_quant(const void* x0, const void* x1, int64_t T, int64_t H,
+                                  int64_t D, const float* scale0, const float* scale1,
+                                  int64_t scale_stride, const int64_t* slot, uint8_t* cache0,
+                                  uint8_t* cache1, int64_t n_slots, int num_sms,
+                                  cudaStream_t st);
 
 // RMSNorm fused with the per-token quantizer (norm_quant.cu); K <= 65536.
 // y (optional) receives the bf16 normalised rows, [R, K] contiguous.

@@ -246,6 +246,24 @@ FP8_API fp8_status_t fp8_kv_cache_quant(const void* kv_bf16, int64_t T, int64_t 
                                         int64_t n_slots, void* stream);
 
 /*
+ * A layer's keys and values written in one launch: exactly
+ *   fp8_kv_cache_quant(k_bf16, T, H, D, k_scale, scale_stride, slot_mapping,
+ *                      k_cache, n_slots, stream) and
+ *   fp8_kv_cache_quant(v_bf16, T, H, D, v_scale, scale_stride, slot_mapping,
+ *                      v_cache, n_slots, stream)
+ * with the same slots (the cache holds keys and values per layer, "FP8
+ * Inference Explained, in depth", "FP8 KV cache"; an engine writes both at
+ * once, "Quantization: FP8 inference and KV-cache quantization", "Turning it
+ * on in an engine").  Arguments and requirements as above, for each of the
+ * two tensors; k_cache and v_cache must not overlap.
+ */
+FP8_API fp8_status_t fp8_kv_cache_quant_kv(const void* k_bf16, const void* v_bf16, int64_t T,
+                                           int64_t H, int64_t D, const float* k_scale,
+                                           const float* v_scale, int64_t scale_stride,
+                                           const int64_t* slot_mapping, uint8_t* k_cache,
+                                           uint8_t* v_cache, int64_t n_slots, void* stream);
+
+/*
  * Block-wise scales.  Source: "FP8 Quantization", "Granularity" (per-block:
  * one scale per 128 x 128 weight tile) and "FP8 Inference Explained, in
  * depth", "Inside a quantized linear layer" (block-wise scales vary along k,

@@ -124,6 +124,17 @@ def test_host_checks_of_the_scale_variants(L):
     assert L.fp8_kv_cache_quant(fake, 4, 8, 128, fake + 2, 1, None, fake, 16, None) == UNSUP
     assert L.fp8_kv_cache_quant(fake, 0, 8, 128, fake, 1, None, fake, 16, None) == 0
     assert L.fp8_kv_cache_quant(fake, 4, 8, 128, fake, 1, None, fake, 0, None) == 0
+    # keys and values: k, v, T, H, D, k_scale, v_scale, stride, slot, k_cache, v_cache, n, stream
+    kv2 = L.fp8_kv_cache_quant_kv
+    assert kv2(fake, None, 4, 8, 128, fake, fake, 1, None, fake, fake, 16, None) == INVALID
+    assert kv2(fake, fake, 4, 8, 128, fake, None, 1, None, fake, fake, 16, None) == INVALID
+    assert kv2(fake, fake, 4, 8, 128, fake, fake, 1, None, fake, None, 16, None) == INVALID
+    assert kv2(fake, fake, 4, 8, 24, fake, fake, 1, None, fake, fake, 16, None) == UNSUP
+    assert kv2(fake, fake + 8, 4, 8, 128, fake, fake, 1, None, fake, fake, 16, None) == UNSUP
+    assert kv2(fake, fake, 4, 8, 128, fake, fake + 2, 1, None, fake, fake, 16, None) == UNSUP
+    assert kv2(fake, fake, 4, 8, 128, fake, fake, 1, None, fake, fake + 8, 16, None) == UNSUP
+    assert kv2(fake, fake, -1, 8, 128, fake, fake, 1, None, fake, fake, 16, None) == INVALID
+    assert kv2(fake, fake, 0, 8, 128, fake, fake, 1, None, fake, fake, 16, None) == 0
 
 
 def test_host_checks_of_the_blockwise_calls(L):

@@ -235,6 +235,38 @@ def test_kv_cache_per_head_scales_paged_slots(oracle_mod, T):
     kv_case(oracle_mod, T, H, D, scale, slots, n_slots, T + 1)
 
 
+@pytest.mark.parametrize("T,H,D,per_head", [(1, 8, 128, True), (33, 8, 128, True),
+                                             (4096, 8, 128, True), (17, 3, 64, False),
+                                             (9, 40, 80, True)])
+def test_kv_cache_keys_and_values_in_one_launch(oracle_mod, T, H, D, per_head):
+    # both caches must equal two separate writes with the same slots
+    n_slots = 2 * T + 16
+    rng = np.random.default_rng(T * 3 + H)
+    slots = rng.permutation(n_slots)[:T].astype(np.int64)
+    slots[:: 5] = -1
+    slots[1:: 11] = n_slots + 3        # beyond the cache: skipped
+    if per_head:
+        ks = np.exp2(rng.uniform(-3, 2, H)).astype(np.float32)
+        vs = np.exp2(rng.uniform(-3, 2, H)).astype(np.float32)
+    else:
+        ks, vs = np.float32(0.75), np.float32(1.0)
+    k, v = randn((T, H, D), T + 5, 4.0), randn((T, H, D), T + 6, 2.0)
+    kc = torch.full((n_slots, H, D), 0xAB, dtype=torch.uint8, device=DEV)
+    vc = torch.full((n_slots, H, D), 0xCD, dtype=torch.uint8, device=DEV)
+    dev_sc = lambda a: torch.tensor(np.atleast_1d(np.asarray(a, np.float32)), device=DEV)
+    pkg.fp8_kv_cache_quant_kv(k, v, dev_sc(ks), dev_sc(vs), kc, vc,
+                              torch.tensor(slots, device=DEV))
+    torch.cuda.synchronize()
+    assert pkg.fp8_device_status() == 0
+    written = sorted({int(r) for r in slots if 0 <= r < n_slots})
+    untouched = [r for r in range(n_slots) if r not in set(written)]
+    k_ref = oracle_mod.kv_cache_quant_bf16(bits(k), ks, slots, n_slots)
+    v_ref = oracle_mod.kv_cache_quant_bf16(bits(v), vs, slots, n_slots)
+    assert_codes(kc[written], k_ref[written], "keys")
+    assert_codes(vc[written], v_ref[written], "values")
+    assert np.all(host(kc)[untouched] == 0xAB) and np.all(host(vc)[untouched] == 0xCD)
+
+
 @pytest.mark.parametrize("T,H,D", [(64, 8, 128), (5, 1, 16), (17, 3, 64), (9, 40, 80)])
 def test_kv_cache_per_tensor_scale_identity_slots(oracle_mod, T, H, D):
     kv_case(oracle_mod, T, H, D, 1.0, None, T + 3, T * H + D)
