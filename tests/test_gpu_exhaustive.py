@@ -101,3 +101,26 @@ def test_quotients_at_rounding_boundaries(oracle_mod):
     near = np.min(np.abs(quot[:, None].astype(np.float64) - targets[None, :]) /
                   targets[None, :], axis=1)
     assert np.mean(near < 2.0 ** -20) > 0.9
+
+
+@pytest.mark.parametrize("s_val", [1.0, 0.0123, 3.0e-5, 700.0])
+def test_keys_and_values_every_bf16_pattern(oracle_mod, s_val):
+    # the one-launch keys-and-values write over all 65536 bf16 patterns (the
+    # values are the patterns in reverse order, with their own scale)
+    pat = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    H, D = 8, 128
+    T = 65536 // (H * D)
+    k_bits = pat.reshape(T, H, D)
+    v_bits = pat[::-1].copy().reshape(T, H, D)
+    k = torch.from_numpy(k_bits.view(np.int16)).view(torch.bfloat16).to(DEV)
+    v = torch.from_numpy(v_bits.view(np.int16)).view(torch.bfloat16).to(DEV)
+    ks = np.float32(s_val)
+    vs = np.float32(s_val * 0.75)
+    kc = torch.zeros((T, H, D), dtype=torch.uint8, device=DEV)
+    vc = torch.zeros((T, H, D), dtype=torch.uint8, device=DEV)
+    pkg.fp8_kv_cache_quant_kv(k, v, torch.tensor([ks], device=DEV), torch.tensor([vs], device=DEV),
+                              kc, vc)
+    torch.cuda.synchronize()
+    assert pkg.fp8_device_status() == 0
+    assert np.array_equal(host(kc), oracle_mod.kv_cache_quant_bf16(k_bits, ks, None, T))
+    assert np.array_equal(host(vc), oracle_mod.kv_cache_quant_bf16(v_bits, vs, None, T))
