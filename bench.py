@@ -837,7 +837,7 @@ def run_case(spec: str, reps: int = 4):
     build.build()
     dev = torch.device("cuda", 0)
     kind, *dims = spec.split(",")
-    if kind in ("static", "tensor", "kv", "norm"):
+    if kind in ("static", "tensor", "kv", "kvkv", "norm"):
         return run_variant_case(pkg, workloads, dev, kind, [int(v) for v in dims], reps)
     if kind == "block":
         M, K, N = (int(v) for v in dims)
@@ -875,8 +875,8 @@ def run_case(spec: str, reps: int = 4):
 
 
 def run_variant_case(pkg, workloads, dev, kind, dims, reps):
-    """static,M,K / tensor,M,K / norm,M,K / kv,T,H,D: one quantizer variant
-    `reps` times."""
+    """static,M,K / tensor,M,K / norm,M,K / kv,T,H,D / kvkv,T,H,D: one
+    quantizer variant `reps` times."""
     import torch
     if kind == "norm":
         M, K = dims
@@ -892,6 +892,15 @@ def run_variant_case(pkg, workloads, dev, kind, dims, reps):
         slots = torch.randperm(T + 1024)[:T].to(torch.int64).to(dev)
         sc = torch.linspace(0.25, 2.0, H, dtype=torch.float32, device=dev)
         run = lambda: pkg.fp8_kv_cache_quant(kv, sc, cache, slots)
+    elif kind == "kvkv":
+        T, H, D = dims
+        k = workloads.student_t_outliers(T * H, D, workloads.SEED_PREFILL, dev).view(T, H, D)
+        v = workloads.student_t_outliers(T * H, D, workloads.SEED_PREFILL + 1, dev).view(T, H, D)
+        kc = torch.zeros((T + 1024, H, D), dtype=torch.uint8, device=dev)
+        vc = torch.zeros((T + 1024, H, D), dtype=torch.uint8, device=dev)
+        slots = torch.randperm(T + 1024)[:T].to(torch.int64).to(dev)
+        sc = torch.linspace(0.25, 2.0, H, dtype=torch.float32, device=dev)
+        run = lambda: pkg.fp8_kv_cache_quant_kv(k, v, sc, sc, kc, vc, slots)
     else:
         M, K = dims
         x = workloads.student_t_outliers(M, K, workloads.SEED_PREFILL, dev)
@@ -921,8 +930,8 @@ def main():
                     help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--case", default=None,
                     help="M,K,N: run fp8_linear on that one layer a few times and exit; "
-                         "static,M,K / tensor,M,K / norm,M,K / kv,T,H,D: one quantizer "
-                         "variant; "
+                         "static,M,K / tensor,M,K / norm,M,K / kv,T,H,D / kvkv,T,H,D: one "
+                         "quantizer variant; "
                          "block,M,K,N: fp8_linear_blockwise on one layer")
     args = ap.parse_args()
     if args.case:
