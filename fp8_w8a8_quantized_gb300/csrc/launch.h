@@ -14,6 +14,12 @@ namespace fp8k {
 // Per-row dynamic E4M3 quantization (quant.cu).  R > 0, K % 16 == 0.
 cudaError_t launch_quant_rows(const void* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q,
                               int64_t ldq, float* s, cudaStream_t st);
+// The same row layout with the scale *s_given for every row (static scale);
+// K > 0; s_rows (optional) receives the scale per row.  Rows longer than
+// the register path holds: cudaErrorNotSupported.
+cudaError_t launch_quant_rows_given(const void* x, int64_t R, int64_t K, int64_t ldx,
+                                    uint8_t* q, int64_t ldq, const float* s_given, float* s_rows,
+                                    cudaStream_t st);
 
 // Everything a scaled-GEMM launch needs.  xq [M, K] and wq [N, K] are
 // contiguous E4M3, y [M, N] contiguous bf16.

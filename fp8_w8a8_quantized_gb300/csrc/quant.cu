@@ -73,10 +73,14 @@ __device__ __forceinline__ float group_max(float m, float* red) {
     return m;
 }
 
-template <int G, int VPT>
+// kGiven: the scale is *s_given for every row (a static, calibrated scale:
+// no maximum is taken, and quotients beyond 448 saturate); s (optional, may
+// be null) receives it per row.
+template <int G, int VPT, bool kGiven = false>
 __global__ void __launch_bounds__(G > kBlock ? G : kBlock)
     quant_rows_regs(const uint16_t* __restrict__ x, int64_t R, int64_t K, int64_t ldx,
-                    uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s) {
+                    uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ s,
+                    const float* __restrict__ s_given = nullptr) {
     constexpr int B = G > kBlock ? G : kBlock;
     constexpr int ROWS = B / G;
     __shared__ float red[B / 32];
@@ -101,11 +105,16 @@ __global__ void __launch_bounds__(G > kBlock ? G : kBlock)
         if (live && c < C) {
             v[i][0] = ld_stream(xr + 2 * c);
             v[i][1] = ld_stream(xr + 2 * c + 1);
-            m = amax8(v[i][1], amax8(v[i][0], m));
+            if constexpr (!kGiven) m = amax8(v[i][1], amax8(v[i][0], m));
         }
     }
-    m = group_max<G, B>(m, red);
-    const float sc = scale_of(m);
+    float sc;
+    if constexpr (kGiven) {
+        sc = __ldg(s_given);
+    } else {
+        m = group_max<G, B>(m, red);
+        sc = scale_of(m);
+    }
     if (!live) return;
     const Divisor dv = divisor_of(sc);
     uint4* qr = reinterpret_cast<uint4*>(q + row * ldq);
@@ -113,12 +122,12 @@ __global__ void __launch_bounds__(G > kBlock ? G : kBlock)
     for (int i = 0; i < VPT; ++i) {
         const int64_t c = t + static_cast<int64_t>(i) * G;
         if (c < C) {
-            const uint2 a = quant8<true>(v[i][0], dv);
-            const uint2 b = quant8<true>(v[i][1], dv);
+            const uint2 a = quant8<!kGiven>(v[i][0], dv);
+            const uint2 b = quant8<!kGiven>(v[i][1], dv);
             qr[c] = make_uint4(a.x, a.y, b.x, b.y);
         }
     }
-    if (t == 0) s[row] = sc;
+    if (t == 0 && s) s[row] = sc;
 }
 
 // Rows longer than the register path holds: stream the row twice (the
@@ -178,16 +187,58 @@ cudaError_t launch_pdl(void (*kernel)(Params...), int64_t grid, int block, cudaS
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-template <int G, int VPT>
+template <int G, int VPT, bool kGiven = false>
 cudaError_t launch_regs(const uint16_t* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q,
-                        int64_t ldq, float* s, cudaStream_t st) {
+                        int64_t ldq, float* s, cudaStream_t st, const float* s_given = nullptr) {
     constexpr int B = G > kBlock ? G : kBlock;
     constexpr int ROWS = B / G;
     const int64_t grid = (R + ROWS - 1) / ROWS;
-    return launch_pdl(quant_rows_regs<G, VPT>, grid, B, st, x, R, K, ldx, q, ldq, s);
+    return launch_pdl(quant_rows_regs<G, VPT, kGiven>, grid, B, st, x, R, K, ldx, q, ldq, s,
+                      s_given);
+}
+
+// The launch for rows of K = 16 C values: small problems (decode batches)
+// one chunk per thread, large ones kVPT (four for rows longer than 32768).
+// Returns cudaErrorNotSupported for rows longer than the register path holds.
+template <bool kGiven>
+cudaError_t dispatch_regs(const uint16_t* xb, int64_t R, int64_t K, int64_t ldx, uint8_t* q,
+                          int64_t ldq, float* s, const float* s_given, cudaStream_t st) {
+    const int64_t C = K / 16;
+    if (R * C <= kLatencyChunks) {
+        if (C <= 32) return launch_regs<32, 1, kGiven>(xb, R, K, ldx, q, ldq, s, st, s_given);
+        if (C <= 64) return launch_regs<64, 1, kGiven>(xb, R, K, ldx, q, ldq, s, st, s_given);
+        if (C <= 128) return launch_regs<128, 1, kGiven>(xb, R, K, ldx, q, ldq, s, st, s_given);
+        if (C <= 256) return launch_regs<256, 1, kGiven>(xb, R, K, ldx, q, ldq, s, st, s_given);
+        if (C <= 512) return launch_regs<512, 1, kGiven>(xb, R, K, ldx, q, ldq, s, st, s_given);
+        if (C <= 1024) return launch_regs<1024, 1, kGiven>(xb, R, K, ldx, q, ldq, s, st, s_given);
+        if (C <= 2048) return launch_regs<1024, 2, kGiven>(xb, R, K, ldx, q, ldq, s, st, s_given);
+    }
+    if (C <= 32 * kVPT) return launch_regs<32, kVPT, kGiven>(xb, R, K, ldx, q, ldq, s, st, s_given);
+    if (C <= 64 * kVPT) return launch_regs<64, kVPT, kGiven>(xb, R, K, ldx, q, ldq, s, st, s_given);
+    if (C <= 128 * kVPT)
+        return launch_regs<128, kVPT, kGiven>(xb, R, K, ldx, q, ldq, s, st, s_given);
+    if (C <= 256 * kVPT)
+        return launch_regs<256, kVPT, kGiven>(xb, R, K, ldx, q, ldq, s, st, s_given);
+    if (C <= 512 * kVPT)
+        return launch_regs<512, kVPT, kGiven>(xb, R, K, ldx, q, ldq, s, st, s_given);
+    if (C <= 1024 * kVPT)
+        return launch_regs<1024, kVPT, kGiven>(xb, R, K, ldx, q, ldq, s, st, s_given);
+    if (C <= 1024 * 4) return launch_regs<1024, 4, kGiven>(xb, R, K, ldx, q, ldq, s, st, s_given);
+    return cudaErrorNotSupported;
 }
 
 }  // namespace
+
+// Rows with a given scale (the static quantizer): the row layout of the
+// per-token quantizer without its maximum.  Rows longer than the register
+// path holds return cudaErrorNotSupported (the caller's grid-stride kernel
+// takes them).  Preconditions as below, and K > 0; s_rows may be null.
+cudaError_t launch_quant_rows_given(const void* x, int64_t R, int64_t K, int64_t ldx,
+                                    uint8_t* q, int64_t ldq, const float* s_given, float* s_rows,
+                                    cudaStream_t st) {
+    return dispatch_regs<true>(static_cast<const uint16_t*>(x), R, K, ldx, q, ldq, s_rows,
+                               s_given, st);
+}
 
 // Host launcher.  Preconditions (checked by the caller): R > 0, K % 16 == 0,
 // 16-byte aligned rows, R < 2^31.
@@ -195,23 +246,8 @@ cudaError_t launch_quant_rows(const void* x, int64_t R, int64_t K, int64_t ldx, 
                               int64_t ldq, float* s, cudaStream_t st) {
     const uint16_t* xb = static_cast<const uint16_t*>(x);
     if (K == 0) return launch_pdl(fill_ones, (R + 255) / 256, 256, st, s, R);
-    const int64_t C = K / 16;
-    if (R * C <= kLatencyChunks) {
-        if (C <= 32) return launch_regs<32, 1>(xb, R, K, ldx, q, ldq, s, st);
-        if (C <= 64) return launch_regs<64, 1>(xb, R, K, ldx, q, ldq, s, st);
-        if (C <= 128) return launch_regs<128, 1>(xb, R, K, ldx, q, ldq, s, st);
-        if (C <= 256) return launch_regs<256, 1>(xb, R, K, ldx, q, ldq, s, st);
-        if (C <= 512) return launch_regs<512, 1>(xb, R, K, ldx, q, ldq, s, st);
-        if (C <= 1024) return launch_regs<1024, 1>(xb, R, K, ldx, q, ldq, s, st);
-        if (C <= 2048) return launch_regs<1024, 2>(xb, R, K, ldx, q, ldq, s, st);
-    }
-    if (C <= 32 * kVPT) return launch_regs<32, kVPT>(xb, R, K, ldx, q, ldq, s, st);
-    if (C <= 64 * kVPT) return launch_regs<64, kVPT>(xb, R, K, ldx, q, ldq, s, st);
-    if (C <= 128 * kVPT) return launch_regs<128, kVPT>(xb, R, K, ldx, q, ldq, s, st);
-    if (C <= 256 * kVPT) return launch_regs<256, kVPT>(xb, R, K, ldx, q, ldq, s, st);
-    if (C <= 512 * kVPT) return launch_regs<512, kVPT>(xb, R, K, ldx, q, ldq, s, st);
-    if (C <= 1024 * kVPT) return launch_regs<1024, kVPT>(xb, R, K, ldx, q, ldq, s, st);
-    if (C <= 1024 * 4) return launch_regs<1024, 4>(xb, R, K, ldx, q, ldq, s, st);
+    const cudaError_t e = dispatch_regs<false>(xb, R, K, ldx, q, ldq, s, nullptr, st);
+    if (e != cudaErrorNotSupported) return e;
     return launch_pdl(quant_rows_stream, R, 1024, st, xb, R, K, ldx, q, ldq, s);
 }
 

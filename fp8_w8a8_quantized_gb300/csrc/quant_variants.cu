@@ -410,6 +410,12 @@ int64_t grid_for(int64_t chunks, int num_sms) {
 cudaError_t launch_quant_given_scale(const void* x, int64_t R, int64_t K, int64_t ldx,
                                      const float* s, uint8_t* q, int64_t ldq, float* s_rows,
                                      int num_sms, cudaStream_t st) {
+    // rows held in registers, as the per-token quantizer (measured faster than
+    // the grid-stride loop); the loop takes empty and very long rows
+    if (K > 0) {
+        const cudaError_t e = launch_quant_rows_given(x, R, K, ldx, q, ldq, s, s_rows, st);
+        if (e != cudaErrorNotSupported) return e;
+    }
     return launch(quant_given_scale, grid_for(R * (K >> 4), num_sms), st,
                   static_cast<const uint16_t*>(x), R, K, ldx, s, q, ldq, s_rows);
 }
