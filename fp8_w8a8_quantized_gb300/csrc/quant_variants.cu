@@ -8,10 +8,12 @@
 //   * FP8 KV-cache writes with a per-tensor or per-head scale, scattered to
 //     cache slots ("Quantization: FP8 inference and KV-cache quantization",
 //     "Turning it on in an engine").
-// The arithmetic is that of the per-token quantizer (quant_math.cuh).  All
-// are grid-stride loops over 16-element chunks (one 32-byte load, one 16-byte
-// store), memory-bound; contiguous tensors take a flat loop with no row
-// arithmetic and two chunks in flight per thread.  The per-tensor amax is two
+// The arithmetic is that of the per-token quantizer (quant_math.cuh).  The
+// static scale runs in the per-token quantizer's row layout (quant.cu) and
+// falls back to the grid-stride loop here for empty or very long rows; the
+// others are grid-stride loops over 16-element chunks (one 32-byte load, one
+// 16-byte store), memory-bound; contiguous tensors take a flat loop with no
+// row arithmetic and two chunks in flight per thread.  The per-tensor amax is two
 // launches (per-CTA maxima, then every CTA reduces them), which needs no
 // atomics and no zeroed memory; the first pass reads x with an L2
 // evict-last hint and the second reads it back from the end, so that much of
