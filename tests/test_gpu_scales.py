@@ -235,6 +235,24 @@ def test_kv_cache_per_head_scales_paged_slots(oracle_mod, T):
     kv_case(oracle_mod, T, H, D, scale, slots, n_slots, T + 1)
 
 
+def test_kv_cache_keys_and_values_identity_slots(oracle_mod):
+    # no slot mapping (token t -> row t), one head of 16, a cache with spare rows
+    T, H, D, n_slots = 5, 1, 16, 8
+    k, v = randn((T, H, D), 71, 3.0), randn((T, H, D), 72, 0.5)
+    kc = torch.full((n_slots, H, D), 0xAB, dtype=torch.uint8, device=DEV)
+    vc = torch.full((n_slots, H, D), 0xCD, dtype=torch.uint8, device=DEV)
+    ks = torch.tensor([0.02], device=DEV)
+    vs = torch.tensor([1.0], device=DEV)
+    pkg.fp8_kv_cache_quant_kv(k, v, ks, vs, kc, vc)
+    torch.cuda.synchronize()
+    assert pkg.fp8_device_status() == 0
+    k_ref = oracle_mod.kv_cache_quant_bf16(bits(k), np.float32(0.02), None, n_slots)
+    v_ref = oracle_mod.kv_cache_quant_bf16(bits(v), np.float32(1.0), None, n_slots)
+    assert_codes(kc[:T], k_ref[:T], "keys")
+    assert_codes(vc[:T], v_ref[:T], "values")
+    assert np.all(host(kc)[T:] == 0xAB) and np.all(host(vc)[T:] == 0xCD)
+
+
 @pytest.mark.parametrize("T,H,D,per_head", [(1, 8, 128, True), (33, 8, 128, True),
                                              (4096, 8, 128, True), (17, 3, 64, False),
                                              (9, 40, 80, True)])
