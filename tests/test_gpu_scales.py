@@ -45,6 +45,19 @@ def test_static_scale(oracle_mod, M, K, s_val):
     assert np.all(host(s_rows) == s32)
 
 
+@pytest.mark.parametrize("M,K", [(3, 65536), (2, 65552), (2, 131072)])
+def test_static_scale_long_rows(oracle_mod, M, K):
+    # the longest rows the register layout holds (4096 chunks), and rows
+    # beyond it (the grid-stride loop)
+    x = workloads.gaussian_outliers(M, K, 17, DEV)
+    s = torch.tensor([0.0123], dtype=torch.float32, device=DEV)
+    s_rows = torch.full((M,), -1.0, dtype=torch.float32, device=DEV)
+    q = pkg.fp8_quant_static(x, s, s_rows=s_rows)
+    torch.cuda.synchronize()
+    assert_codes(q, oracle_mod.quant_rows_scaled_bf16(bits(x), np.float32(0.0123)), "static long")
+    assert np.all(host(s_rows) == np.float32(0.0123))
+
+
 def test_static_scale_saturates_and_strides(oracle_mod):
     # a scale far too small for the data: most codes clip to +-448
     M, K, ldx, ldq = 37, 512, 520, 544
