@@ -23,8 +23,7 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libfp8w8a8.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
 
-SOURCES = ["api.cu", "quant.cu", "quant_variants.cu", "norm_quant.cu", "gemm_prefill.cu",
-           "gemm_pair.cu", "gemm_decode.cu", "gemm_blockwise.cu", "noalloc.cu",
+SOURCES = ["api.cu", "quant.cu", "quant_variants.cu", "norm_quant.cu", "gemm_pair.cu", "gemm_decode.cu", "gemm_blockwise.cu", "noalloc.cu",
            "selftest.cu"]
 HEADERS = ["ptx.cuh", "launch.h", "quant_math.cuh", "decode_common.cuh"]
 

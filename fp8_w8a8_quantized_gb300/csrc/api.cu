@@ -2,8 +2,8 @@
 //
 // This file only validates arguments on the host, keeps a little per-device
 // state (SM count, the device status word, kernel attributes) and launches
-// the kernels of quant.cu, quant_variants.cu, norm_quant.cu, gemm_prefill.cu,
-// gemm_pair.cu, gemm_decode.cu and gemm_blockwise.cu.  It never
+// the kernels of quant.cu, quant_variants.cu, norm_quant.cu, gemm_pair.cu,
+// gemm_decode.cu and gemm_blockwise.cu.  It never
 // allocates device memory and never synchronizes, except in
 // fp8_device_status().
 #include <cuda.h>
@@ -53,7 +53,6 @@ fp8_status_t current_device(DeviceState** out) {
             d.verdict = FP8_ERR_UNSUPPORTED;
         } else if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word) !=
                        cudaSuccess ||
-                   fp8k::prepare_gemm_prefill() != cudaSuccess ||
                    fp8k::prepare_gemm_decode() != cudaSuccess ||
                    fp8k::prepare_gemm_blockwise() != cudaSuccess ||
                    fp8k::prepare_gemm_pair() != cudaSuccess) {
@@ -153,8 +152,7 @@ fp8_status_t run_gemm(const uint8_t* xq, const float* s_tok, const uint8_t* wq, 
     a.stream = static_cast<cudaStream_t>(stream);
     cudaError_t e = blockwise                 ? fp8k::launch_gemm_blockwise(a)
                     : M <= fp8k::kDecodeMaxM ? fp8k::launch_gemm_decode(a)
-                    : M >= fp8k::kPairMinM   ? fp8k::launch_gemm_pair(a)
-                                             : fp8k::launch_gemm_prefill(a);
+                                             : fp8k::launch_gemm_pair(a);
     return e == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 

@@ -1,12 +1,12 @@
-// Scaled FP8 GEMM for large M on pairs of SMs (tcgen05 cta_group::2).
+// Scaled FP8 GEMM for every M above the decode sizes, on pairs of SMs
+// (tcgen05 cta_group::2).
 //
 //   y[m, n] = bf16_rn((acc[m, n] * s_tok[m]) * s_w[n]),
 //   acc[m, n] = sum_k e4m3(xq[m, k]) * e4m3(wq[n, k])      (fp32, in TMEM)
 //
-// Same result as gemm_prefill.cu ("FP8 Inference Explained, in depth",
-// "Inside a quantized linear layer"; "FP8 Quantization", "How FP8 Matmul
-// Works at the Hardware Level"), with a 256 x 256 output tile per cluster of
-// two CTAs on two SMs.  One MMA instruction (M = 256, N = 256, K = 32) runs on
+// ("FP8 Inference Explained, in depth", "Inside a quantized linear layer";
+// "FP8 Quantization", "How FP8 Matmul Works at the Hardware Level"), with a
+// 256 x 256 output tile per cluster of two CTAs on two SMs.  One MMA instruction (M = 256, N = 256, K = 32) runs on
 // both SMs' tensor cores: each CTA holds its own 128 rows of the activation
 // tile and half of the weight tile, so per SM and per 128 of K, TMA writes
 // 32 KB into shared memory instead of the 48 KB a one-SM 128 x 256 tile

@@ -46,17 +46,14 @@ struct GemmArgs {
 bool encode_tmap_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint64_t ld_bytes, uint32_t box_cols, uint32_t box_rows);
 
-// Persistent 128x256-tile tcgen05 GEMM for large M (gemm_prefill.cu).
-cudaError_t launch_gemm_prefill(const GemmArgs& a);
+// Weight-streaming split-K tcgen05 GEMM for M <= kDecodeMaxM (gemm_decode.cu).
+constexpr int kDecodeMaxM = 64;
 
 // Persistent 256x256-tile GEMM on pairs of SMs (tcgen05 cta_group::2) for
-// M >= kPairMinM (gemm_pair.cu).
-constexpr int kPairMinM = 256;
+// every larger M (gemm_pair.cu).
 cudaError_t launch_gemm_pair(const GemmArgs& a);
 int gemm_pair_resident_clusters(int num_sms);
 
-// Weight-streaming split-K tcgen05 GEMM for M <= 64 (gemm_decode.cu).
-constexpr int kDecodeMaxM = 64;
 cudaError_t launch_gemm_decode(const GemmArgs& a);
 // How many clusters of `size` decode-GEMM CTAs can be resident at once (a
 // cluster must fit on the SMs of one GPC); 0 if unknown.
@@ -111,7 +108,6 @@ fp8_status_t linear_checks(const void* x, const uint8_t* wq, const float* s_w, c
                            int64_t M, int64_t N, int64_t K);
 
 // One-time per-device kernel attribute setup (dynamic shared memory limits).
-cudaError_t prepare_gemm_prefill();
 cudaError_t prepare_gemm_decode();
 cudaError_t prepare_gemm_blockwise();
 cudaError_t prepare_gemm_pair();

@@ -1,7 +1,7 @@
-"""GPU parity of the scaled FP8 GEMM (all three kernels: the weight-streaming
-split-K kernel for M <= 64, the one-SM persistent tile kernel up to M = 255
-and the paired-SM 256 x 256 tile kernel above), fed with the oracle's own
-codes and scales, against the oracle's fp64 result."""
+"""GPU parity of the scaled FP8 GEMM (both kernels: the weight-streaming
+split-K kernel for M <= 64 and the paired-SM 256 x 256 tile kernel above,
+partial row tiles included), fed with the oracle's own codes and scales,
+against the oracle's fp64 result."""
 import numpy as np
 import pytest
 import torch
@@ -50,14 +50,15 @@ def test_random_codes(oracle_mod, M, N, K):
     check_rows(y, ref, f"gemm {M}x{N}x{K}")
 
 
-# Persistent kernels walking more than one output tile per CTA (or per CTA
-# pair): the second TMEM accumulator buffer, its phase flips and the tile
-# walk.  The one-SM kernel (65 <= M < 256) runs min(tiles, 152) CTAs of
-# 128 x 256 tiles; the paired-SM kernel (M >= 256) at most 76 pairs of
-# 256 x 256 tiles.  Full outputs against the oracle.
+# The persistent paired-SM kernel walking more than one output tile per CTA
+# pair (at most 76 pairs of 256 x 256 tiles): the second TMEM accumulator
+# buffer, its phase flips and the tile walk; below 256 rows the tile's rows
+# past M (for M <= 128 the whole second CTA's half) are zero-filled by
+# TMA and never stored.  Full outputs against the oracle.
 MULTI_TILE = [
-    (200, 28672, 1024),   # one-SM: 2 x 112 = 224 tiles, up to 2 per CTA
-    (255, 49152, 256),    # one-SM: 2 x 192 = 384 tiles, up to 3 per CTA
+    (200, 28672, 1024),   # paired: 1 x 112 = 112 tiles, up to 2 per pair
+    (255, 49152, 256),    # paired: 1 x 192 = 192 tiles, up to 3 per pair
+    (80, 24576, 512),     # paired: 1 x 96 tiles, rows 80-255 of each tile empty
     (1024, 8192, 1024),   # paired: 4 x 32 = 128 tiles, up to 2 per pair
     (1536, 8192, 256),    # paired: 6 x 32 = 192 tiles, up to 3 per pair
     (2304, 4864, 272),    # paired: 9 x 19 = 171 tiles, ragged K

@@ -80,7 +80,7 @@ def test_scratch_codes_and_scales_through_a_one_hot_layer(oracle_mod):
     wq = torch.zeros(N, K, dtype=torch.uint8, device=DEV)
     wq[torch.arange(N), torch.arange(N)] = 0x38
     s_w = torch.ones(N, dtype=torch.float32, device=DEV)
-    for M, seed in [(24, 7), (80, 8)]:          # decode kernel, then one-SM kernel
+    for M, seed in [(24, 7), (80, 8)]:          # decode kernel, then paired-SM kernel
         x = workloads.gaussian_outliers(M, K, seed, DEV)
         y = run(f, x, wq, s_w, N)
         qx, s_tok = oracle_mod.quant_rows_bf16(bits(x))
