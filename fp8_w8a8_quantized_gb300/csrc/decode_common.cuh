@@ -24,6 +24,7 @@ constexpr int kCtasPerSm = 3;
 constexpr uint32_t kSmemPerSm = 228 * 1024;
 constexpr uint32_t kCtaSmem = kSmemPerSm / kCtasPerSm - 1024;  // 1 KB reserved per CTA
 constexpr uint32_t kCtaSmem2 = kSmemPerSm / 2 - 1024;           // two CTAs per SM
+constexpr uint32_t kCtaSmem1 = kSmemPerSm - 1024;               // one CTA per SM
 constexpr int kL2PrefetchBlocks = 4;  // k-blocks of W prefetched into L2 before the wait (measured)
 
 // Accumulator columns of one warp's 32 TMEM lanes -> registers.
@@ -63,8 +64,9 @@ __host__ __device__ __forceinline__ void split_range(int rank, int nk, int split
 // of S may be resident at once: clusters[S], when known, is that number and
 // sets the waves (measured on GB300: 64 clusters of 7 do not fit, 74 of 6
 // do).
-inline int choose_splits(int n_tiles, int nk, int num_sms, const int* clusters = nullptr) {
-    const int slots = kCtasPerSm * num_sms;
+inline int choose_splits(int n_tiles, int nk, int num_sms, const int* clusters = nullptr,
+                         int ctas_per_sm = kCtasPerSm) {
+    const int slots = ctas_per_sm * num_sms;
     int best = 1;
     double best_eff = -1.0;
     for (int s = 1; s <= kMaxSplits; ++s) {

@@ -613,7 +613,7 @@ cudaError_t prepare_gemm_blockwise() {
 cudaError_t launch_gemm_blockwise(const GemmArgs& a) {
     if (a.M <= 16) return dc::launch_mt<16>(a);
     if (a.M <= 32) return dc::launch_mt<32>(a);
-    if (a.M <= kDecodeMaxM) return dc::launch_mt<64>(a);
+    if (a.M <= kBlockwiseDecodeMaxM) return dc::launch_mt<64>(a);
 
     CUtensorMap tmA, tmB;
     if (!encode_tmap_u8(&tmA, a.xq, a.M, a.K, a.K, pf::BK, pf::BM)) return cudaErrorInvalidValue;

@@ -1,6 +1,7 @@
-// Scaled FP8 GEMM for decode-sized M (M <= 64 tokens): weight streaming.
+// Scaled FP8 GEMM for decode-sized and mid-size M (M <= 256 tokens): weight
+// streaming.
 //
-// Same result as the prefill kernel,
+// Same result as the paired-SM kernel (gemm_pair.cu),
 //   y[m, n] = bf16_rn((acc[m, n] * s_tok[m]) * s_w[n]),
 //   acc[m, n] = sum_k e4m3(xq[m, k]) * e4m3(wq[n, k])  (fp32),
 // but at decode batch sizes the layer is bound by reading W once from HBM
@@ -8,12 +9,15 @@
 // speed is set by memory bandwidth), so the kernel is shaped around the weight
 // stream:
 //   * operands swapped: 128 rows of W fill the MMA's M = 128 side and the
-//     tokens (padded to MT = 16/32/64 with TMA zero fill) the narrow N side,
-//     so D^T[n, m] accumulates in TMEM (128 lanes x MT columns);
+//     tokens (padded to MT = 16/32/64/128/256 with TMA zero fill) the N side,
+//     so D^T[n, m] accumulates in TMEM (128 lanes x MT columns); 128- and
+//     256-token tiles (32 and 48 KB ring stages, 64 and 128 KB partials) run
+//     two CTAs or one per SM, the narrower ones kCtasPerSm;
 //   * split-K over a thread-block cluster of S CTAs (one cluster per 128-row
-//     weight slab), sized so that the grid fills every SM with kCtasPerSm
-//     CTAs: several small CTAs per SM keep more independent TMA producers in
-//     flight than one deep ring (measured on GB300);
+//     weight slab), sized so that the grid fills every SM with as many CTAs
+//     as the tile width allows: several small CTAs per SM keep more
+//     independent TMA producers in flight than one deep ring (measured on
+//     GB300);
 //   * each CTA streams its K slice of W through a TMA ring; the X tile of the
 //     same K slice rides along in the same stage;
 //   * each CTA of the cluster owns 128/S rows of the slab's output and sums
@@ -54,6 +58,7 @@ struct Cfg {
     static constexpr uint32_t RED_BYTES = MT * BNW * 4;  // pull: partial D^T in the ring
 };
 
+template <int MT>
 struct Bars {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
@@ -62,7 +67,7 @@ struct Bars {
     uint64_t recv_full;  // push: the S partials of this CTA's rows have arrived
     uint32_t tmem_base;
     int abort;
-    float s_tok[64];   // token scales, staged for the reduction
+    float s_tok[MT < 64 ? 64 : MT];  // token scales, staged for the reduction
     float s_w[BNW];    // weight scales of the rows this CTA reduces
 };
 
@@ -84,10 +89,10 @@ Layout layout_of(int M, int splits, int64_t budget) {
     Layout l;
     l.recv_bytes = PUSH ? push_recv_bytes(M, splits) : 0u;
     const int64_t room =
-        budget - 1024 - static_cast<int64_t>(sizeof(Bars)) - l.recv_bytes;
+        budget - 1024 - static_cast<int64_t>(sizeof(Bars<MT>)) - l.recv_bytes;
     int st = static_cast<int>(room / C::STAGE_BYTES);
     l.stages = st < kMaxStages ? st : kMaxStages;
-    l.smem = 1024 + static_cast<size_t>(l.stages) * C::STAGE_BYTES + l.recv_bytes + sizeof(Bars);
+    l.smem = 1024 + static_cast<size_t>(l.stages) * C::STAGE_BYTES + l.recv_bytes + sizeof(Bars<MT>);
     return l;
 }
 
@@ -105,7 +110,7 @@ __global__ void __launch_bounds__(kThreads)
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     uint8_t* ring = smem;
     float* recv = reinterpret_cast<float*>(smem + stages * C::STAGE_BYTES);  // push
-    Bars* bars = reinterpret_cast<Bars*>(smem + stages * C::STAGE_BYTES + recv_bytes);
+    Bars<MT>* bars = reinterpret_cast<Bars<MT>*>(smem + stages * C::STAGE_BYTES + recv_bytes);
     float* red = reinterpret_cast<float*>(smem);  // pull: [MT][BNW], after the main loop
 
     const int warp = threadIdx.x >> 5;
@@ -235,30 +240,51 @@ __global__ void __launch_bounds__(kThreads)
         }
         const int quarter = warp & 3;
         const int nl = quarter * 32 + lane;
-        float v[MT];
+        const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
         bool have = false;
-        if (nkb > 0) {
-            have = warp_wait(&bars->acc_full, 0, abort_flag, status);
-            if (have) {
-                tc_fence_after();
-                tmem_ld_cols<MT>(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16), v);
+        if constexpr (MT <= 64) {
+            float v[MT];
+            if (nkb > 0) {
+                have = warp_wait(&bars->acc_full, 0, abort_flag, status);
+                if (have) {
+                    tc_fence_after();
+                    tmem_ld_cols<MT>(tacc, v);
+                }
             }
-        }
-        tc_fence_before();
-        if (!have) {
+            tc_fence_before();
+            if (!have) {
 #pragma unroll
-            for (int j = 0; j < MT; ++j) v[j] = 0.0f;
-        }
-        if constexpr (PUSH) {
-            // Sent even after a failed wait (as zeros) so that every owner's
-            // barrier completes.
-            cluster_wait();
-            push_send<MT>(v, M, nl, rank, splits, recv, &bars->recv_full);
+                for (int j = 0; j < MT; ++j) v[j] = 0.0f;
+            }
+            if constexpr (PUSH) {
+                // Sent even after a failed wait (as zeros) so that every
+                // owner's barrier completes.
+                cluster_wait();
+                push_send<MT>(v, M, nl, rank, splits, recv, &bars->recv_full);
+            } else {
+                // The ring is idle once the accumulator is complete (every
+                // stage was consumed by an MMA that has finished): reuse it.
+#pragma unroll
+                for (int j = 0; j < MT; ++j) red[j * BNW + nl] = v[j];
+            }
         } else {
-            // The ring is idle once the accumulator is complete (every stage
-            // was consumed by an MMA that has finished): reuse it.
+            static_assert(!PUSH, "wide token tiles pull");
+            // The same through the idle ring, 32 token columns at a time
+            // (a wide tile's accumulator row would not fit in registers).
+            if (nkb > 0) have = warp_wait(&bars->acc_full, 0, abort_flag, status);
+            if (have) tc_fence_after();
+#pragma unroll 1
+            for (int h = 0; h < MT / 32; ++h) {
+                uint32_t r[32];
+                if (have) {
+                    tmem_ld_32x32b_x32(tacc + h * 32, r);
+                    tmem_ld_wait();
+                }
 #pragma unroll
-            for (int j = 0; j < MT; ++j) red[j * BNW + nl] = v[j];
+                for (int j = 0; j < 32; ++j)
+                    red[(h * 32 + j) * BNW + nl] = have ? __uint_as_float(r[j]) : 0.0f;
+            }
+            tc_fence_before();
         }
     }
 
@@ -299,12 +325,12 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 template <int MT, bool PUSH>
-cudaError_t launch_mt(const GemmArgs& a, int splits, bool two) {
+cudaError_t launch_mt(const GemmArgs& a, int splits, uint32_t budget) {
     CUtensorMap tmW, tmX;
     if (!encode_tmap_u8(&tmW, a.wq, a.N, a.K, a.K, BK, kWBoxRows)) return cudaErrorInvalidValue;
     if (!encode_tmap_u8(&tmX, a.xq, a.M, a.K, a.K, BK, MT)) return cudaErrorInvalidValue;
     const int n_tiles = (a.N + BNW - 1) / BNW;
-    const Layout l = layout_of<MT, PUSH>(a.M, splits, two ? kCtaSmem2 : kCtaSmem);
+    const Layout l = layout_of<MT, PUSH>(a.M, splits, budget);
     if (l.stages < 2 || (!PUSH && Cfg<MT>::RED_BYTES > l.stages * Cfg<MT>::STAGE_BYTES))
         return cudaErrorInvalidConfiguration;
 
@@ -365,13 +391,22 @@ int gemm_decode_resident_clusters(int size) {
 }
 
 cudaError_t prepare_gemm_decode() {
-    for (auto* k :
-         {gemm_decode_kernel<16, true>, gemm_decode_kernel<32, false>, gemm_decode_kernel<64, false>}) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+    struct {
+        const void* k;
+        uint32_t smem;
+    } const kernels[] = {
+        {reinterpret_cast<const void*>(gemm_decode_kernel<16, true>), kCtaSmem2},
+        {reinterpret_cast<const void*>(gemm_decode_kernel<32, false>), kCtaSmem2},
+        {reinterpret_cast<const void*>(gemm_decode_kernel<64, false>), kCtaSmem2},
+        {reinterpret_cast<const void*>(gemm_decode_kernel<128, false>), kCtaSmem2},
+        {reinterpret_cast<const void*>(gemm_decode_kernel<256, false>), kCtaSmem1},
+    };
+    for (const auto& k : kernels) {
+        cudaError_t e = cudaFuncSetAttribute(k.k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                              cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kCtaSmem2));
+        e = cudaFuncSetAttribute(k.k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(k.smem));
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -387,9 +422,18 @@ cudaError_t launch_gemm_decode(const GemmArgs& a) {
     // two-per-SM grids, where the receive buffer fits beside a 4-stage ring,
     // measured 3924 against 3960 GB/s for the step).
     const bool two = static_cast<int64_t>(n_tiles) * splits <= 2 * a.num_sms;
-    if (a.M <= 16) return launch_mt<16, true>(a, splits, two);
-    if (a.M <= 32) return launch_mt<32, false>(a, splits, two);
-    return launch_mt<64, false>(a, splits, two);
+    const uint32_t budget = two ? kCtaSmem2 : kCtaSmem;
+    if (a.M <= 16) return launch_mt<16, true>(a, splits, budget);
+    if (a.M <= 32) return launch_mt<32, false>(a, splits, budget);
+    if (a.M <= 64) return launch_mt<64, false>(a, splits, budget);
+    // Wider token tiles: a 32 KB (128 tokens) or 48 KB (256) ring stage and a
+    // 64 / 128 KB partial, so two CTAs or one share an SM; the split is
+    // chosen for that many CTA slots.
+    const int nk = (a.K + BK - 1) / BK;
+    if (a.M <= 128)
+        return launch_mt<128, false>(a, choose_splits(n_tiles, nk, a.num_sms, nullptr, 2),
+                                     kCtaSmem2);
+    return launch_mt<256, false>(a, choose_splits(n_tiles, nk, a.num_sms, nullptr, 1), kCtaSmem1);
 }
 
 }  // namespace fp8k

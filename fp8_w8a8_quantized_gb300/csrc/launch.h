@@ -46,8 +46,10 @@ struct GemmArgs {
 bool encode_tmap_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint64_t ld_bytes, uint32_t box_cols, uint32_t box_rows);
 
-// Weight-streaming split-K tcgen05 GEMM for M <= kDecodeMaxM (gemm_decode.cu).
-constexpr int kDecodeMaxM = 64;
+// Weight-streaming split-K tcgen05 GEMM for M <= kDecodeMaxM (gemm_decode.cu);
+// the block-scaled variant (gemm_blockwise.cu) up to kBlockwiseDecodeMaxM.
+constexpr int kDecodeMaxM = 256;
+constexpr int kBlockwiseDecodeMaxM = 64;
 
 // Persistent 256x256-tile GEMM on pairs of SMs (tcgen05 cta_group::2) for
 // every larger M (gemm_pair.cu).

@@ -129,9 +129,10 @@ FP8_API fp8_status_t fp8_quant_per_channel_weights(const void* w_bf16, int64_t N
  * Requirements: K % 16 == 0, K > 0; xq, wq, y_bf16 16-byte aligned;
  * M, N, K < 2^31.  The fp32 summation order is fixed for a given shape, so
  * repeated calls give identical bits.
- * Kernel choice: M <= 64 uses the weight-streaming split-K kernel (weights on
- * the 128-row MMA side, tokens on the narrow side), larger M the persistent
- * 256x256-tile kernel that runs each MMA on a pair of SMs (cta_group::2).
+ * Kernel choice: M <= 256 uses the weight-streaming split-K kernel (weights on
+ * the 128-row MMA side, tokens on the other, in tiles of 16, 32, 64, 128 or
+ * 256), larger M the persistent 256x256-tile kernel that runs each MMA on a
+ * pair of SMs (cta_group::2).
  */
 FP8_API fp8_status_t fp8_scaled_gemm(const uint8_t* xq, const float* s_tok, const uint8_t* wq,
                                      const float* s_w, void* y_bf16, int64_t M, int64_t N,

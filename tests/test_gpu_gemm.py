@@ -1,7 +1,7 @@
 """GPU parity of the scaled FP8 GEMM (both kernels: the weight-streaming
-split-K kernel for M <= 64 and the paired-SM 256 x 256 tile kernel above,
-partial row tiles included), fed with the oracle's own codes and scales,
-against the oracle's fp64 result."""
+split-K kernel for M <= 256, token tiles of 16 to 256, and the paired-SM
+256 x 256 tile kernel above, partial row tiles included), fed with the
+oracle's own codes and scales, against the oracle's fp64 result."""
 import numpy as np
 import pytest
 import torch
@@ -52,13 +52,13 @@ def test_random_codes(oracle_mod, M, N, K):
 
 # The persistent paired-SM kernel walking more than one output tile per CTA
 # pair (at most 76 pairs of 256 x 256 tiles): the second TMEM accumulator
-# buffer, its phase flips and the tile walk; below 256 rows the tile's rows
-# past M (for M <= 128 the whole second CTA's half) are zero-filled by
-# TMA and never stored.  Full outputs against the oracle.
+# buffer, its phase flips and the tile walk; rows of a tile past M are
+# zero-filled by TMA and never stored.  And the weight-streaming kernel with
+# wide token tiles over many weight slabs.  Full outputs against the oracle.
 MULTI_TILE = [
-    (200, 28672, 1024),   # paired: 1 x 112 = 112 tiles, up to 2 per pair
-    (255, 49152, 256),    # paired: 1 x 192 = 192 tiles, up to 3 per pair
-    (80, 24576, 512),     # paired: 1 x 96 tiles, rows 80-255 of each tile empty
+    (200, 28672, 1024),   # 256-token tiles, 224 slabs
+    (255, 49152, 256),    # 256-token tiles, 384 slabs, two k-blocks (no K split)
+    (80, 24576, 512),     # 128-token tiles, 48 of 128 token columns empty
     (1024, 8192, 1024),   # paired: 4 x 32 = 128 tiles, up to 2 per pair
     (1536, 8192, 256),    # paired: 6 x 32 = 192 tiles, up to 3 per pair
     (2304, 4864, 272),    # paired: 9 x 19 = 171 tiles, ragged K

@@ -1,10 +1,10 @@
 """GPU parity of the whole W8A8 layer (fp8_linear) on every configuration:
 quantized activation bytes and scales bit-exact (read back from the
 workspace), weight codes and scales bit-exact, outputs within tolerance.
-Small shapes and every decode batch are compared in full; the prefill
-shapes on full output rows of one token from every 128-row block (so every
-row tile of the persistent kernels is checked), with the same launch
-configuration the benchmark times."""
+Small shapes, every decode batch and the mid-size batches of the smaller
+layers are compared in full; the prefill shapes on full output rows of one
+token from every 128-row block (so every row tile of the persistent kernel
+is checked), with the same launch configuration the benchmark times."""
 import numpy as np
 import pytest
 import torch
@@ -56,6 +56,20 @@ def test_decode_8b(oracle_mod, M, name, K, N):
     x = workloads.gaussian_outliers(M, K, workloads.SEED_DECODE, DEV)
     w = workloads.weights(N, K, workloads.SEED_DECODE, DEV)
     layer(oracle_mod, x, w)
+
+
+# Batches between the decode and prefill configurations (serving batches of
+# 64-256 sequences, chunked prefill): the weight-streaming kernel with 128-
+# and 256-token tiles (two CTAs, or one, per SM).  Every output row where
+# the oracle's exact sums stay within a few seconds, else one token from
+# every 16 (and the first and last); activation and weight codes in full.
+@pytest.mark.parametrize("M", [65, 128, 129, 256])
+@pytest.mark.parametrize("name,K,N", workloads.SHAPES_8B)
+def test_mid_batch_8b(oracle_mod, M, name, K, N):
+    x = workloads.gaussian_outliers(M, K, workloads.SEED_DECODE + M, DEV)
+    w = workloads.weights(N, K, workloads.SEED_DECODE, DEV)
+    rows = None if M * N * K <= 16 * 10 ** 9 else tile_rows(M, M + N, block=16)
+    layer(oracle_mod, x, w, rows=rows)
 
 
 @pytest.mark.parametrize("M", workloads.PREFILL_M)
