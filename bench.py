@@ -430,6 +430,7 @@ def run_ours(args):
 
     decode_70b = decode_70b_rates(pkg, workloads, dev, stream, timed, hbm_peak, args.steps, l2)
     prefill_70b = prefill_70b_rate(pkg, workloads, dev, stream, timed, fp8_peak, args.steps)
+    mid_batch = mid_batch_rates(pkg, workloads, dev, stream, timed, hbm_peak, args.steps, l2)
     variants = variant_rates(pkg, workloads, dev, stream, timed, hbm_peak, args.steps)
     blockwise = blockwise_rates(pkg, workloads, dev, stream, timed, hbm_peak, fp8_peak,
                                 args.steps, l2)
@@ -542,6 +543,7 @@ def run_ours(args):
             "scale_variants": variants,
             "decode_70b": decode_70b,
             "prefill_70b": prefill_70b,
+            "mid_batch": mid_batch,
             "blockwise": blockwise,
             "e2e": e2e,
             "cpu_baseline": cpu,
@@ -718,6 +720,61 @@ def decode_70b_rates(pkg, workloads, dev, stream, timed, hbm_peak, steps, l2):
             "workload": "llama-3.1-70b decode linear layers at 32 tokens: (K,N) in "
                         "{(8192,10240),(8192,8192),(8192,57344),(28672,8192)}, 4 fp8_linear "
                         "calls per step"}
+
+
+def mid_batch_rates(pkg, workloads, dev, stream, timed, hbm_peak, steps, l2):
+    """The 8B layers at 128 and 256 tokens (serving batches between the decode
+    and prefill configurations; the weight-streaming GEMM with 128- and
+    256-token tiles): one step = 8 fp8_linear calls in a CUDA graph, weights
+    rotated over sets larger than L2 in total.  TFLOPS and GB/s (context:
+    neither is a configuration the targets name)."""
+    import torch
+
+    calls = [(M, K, N) for M in (128, 256) for (_, K, N) in workloads.SHAPES_8B]
+    per_set = sum(N * K for (_, K, N) in workloads.SHAPES_8B)
+    nsets = max(2, -(-2 * l2 // per_set) + 1)
+    wsets = []
+    for s_ in range(nsets):
+        d = {}
+        for (_, K, N) in workloads.SHAPES_8B:
+            w = workloads.weights(N, K, 1 + 100 * s_, dev)
+            d[(K, N)] = pkg.fp8_quant_per_channel_weights(w)
+            del w
+        wsets.append(d)
+    xs = [workloads.gaussian_outliers(M, K, workloads.SEED_DECODE, dev) for (M, K, N) in calls]
+    ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for (M, K, N) in calls]
+    wss = [torch.empty(pkg.fp8_linear_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+           for (M, K, N) in calls]
+    torch.cuda.synchronize()
+
+    def step(wset, st):
+        for i, (M, K, N) in enumerate(calls):
+            wq, sw = wset[(K, N)]
+            pkg.fp8_linear(xs[i], wq, sw, y=ys[i], workspace=wss[i], stream=st)
+
+    graphs = []
+    with torch.cuda.stream(stream):
+        for wset in wsets:
+            step(wset, stream)
+        stream.synchronize()
+        for wset in wsets:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(wset, torch.cuda.current_stream())
+            graphs.append(g)
+    torch.cuda.synchronize()
+    n = max(steps, 50)
+    t = timed(lambda i: graphs[i % nsets].replay(), n, 3)
+    nbytes = sum(layer_bytes(M, K, N) for (M, K, N) in calls)
+    flops = sum(2 * M * N * K for (M, K, N) in calls)
+    gbs = nbytes * n / t / 1e9
+    del graphs, xs, ys, wss, wsets
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return {"tflops": flops * n / t / 1e12, "gbs": gbs, "frac_of_hbm": gbs / hbm_peak,
+            "ms_per_step": t / n * 1e3,
+            "workload": "llama-3.1-8b linear layers at M in {128, 256}: 8 fp8_linear calls "
+                        "per step"}
 
 
 def variant_rates(pkg, workloads, dev, stream, timed, hbm_peak, steps):
