@@ -28,7 +28,9 @@ struct DeviceState {
     fp8_status_t verdict = FP8_ERR_UNSUPPORTED;
     int num_sms = 0;
     int pair_clusters = 0;  // co-resident clusters of the paired-SM GEMM
-    int decode_clusters[9] = {};  // co-resident clusters of S decode-GEMM CTAs, S = 1..8
+    // co-resident clusters of S decode-GEMM CTAs (S = 1..8) at the footprint
+    // of c = 1..3 CTAs per SM: [(c - 1) * 9 + S]
+    int decode_clusters[27] = {};
     unsigned* status = nullptr;
 };
 
@@ -59,8 +61,10 @@ fp8_status_t current_device(DeviceState** out) {
             d.verdict = FP8_ERR_CUDA;
         } else {
             d.pair_clusters = fp8k::gemm_pair_resident_clusters(d.num_sms);
-            for (int c = 1; c <= 8; ++c)
-                d.decode_clusters[c] = fp8k::gemm_decode_resident_clusters(c);
+            for (int per_sm = 1; per_sm <= 3; ++per_sm)
+                for (int c = 1; c <= 8; ++c)
+                    d.decode_clusters[(per_sm - 1) * 9 + c] =
+                        fp8k::gemm_decode_resident_clusters(c, per_sm);
             d.verdict = FP8_OK;
         }
         d.ready = true;

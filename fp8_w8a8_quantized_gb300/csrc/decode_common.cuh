@@ -83,6 +83,29 @@ inline int choose_splits(int n_tiles, int nk, int num_sms, const int* clusters =
     return best;
 }
 
+// Split count for the wide token tiles (128 and 256 tokens: two CTAs or one
+// per SM, slots = ctas_per_sm x num_sms), whose per-CTA overhead (ring fill,
+// a 64-128 KB partial pulled across the cluster) makes every extra wave
+// expensive: the fewest waves, counted with the clusters of S that can be
+// resident at once (clusters[S] when known, else slots / S), and among
+// those the largest S (at least 2 k-blocks per split).  Measured on the 8B
+// layers at 128 and 256 tokens it picks the fastest S of a 1..8 sweep on
+// every layer, where the busy-slot rule above lost up to 1.7x.
+inline int choose_splits_min_waves(int n_tiles, int nk, int slots, const int* clusters) {
+    int best = 1, best_waves = 1 << 30;
+    for (int s = 1; s <= kMaxSplits; ++s) {
+        if (s > 1 && nk < 2 * s) break;
+        const int per_wave = (clusters && clusters[s] > 0) ? clusters[s] : slots / s;
+        if (per_wave < 1) break;
+        const int waves = (n_tiles + per_wave - 1) / per_wave;
+        if (waves <= best_waves) {
+            best_waves = waves;
+            best = s;
+        }
+    }
+    return best;
+}
+
 // ---------------------------------------------------------------------------
 // Split-K reduction.  Each CTA of a cluster of S owns output rows
 // [lo, lo + width) of the 128-row slab, lo = rank * rows_per with rows_per =

@@ -562,7 +562,8 @@ cudaError_t launch_mt(const GemmArgs& a) {
     if (!encode_tmap_u8(&tmX, a.xq, a.M, a.K, a.K, BK, MT)) return cudaErrorInvalidValue;
     const int n_tiles = (a.N + BNW - 1) / BNW;
     const int nk = (a.K + BK - 1) / BK;
-    const int splits = choose_splits(n_tiles, nk, a.num_sms, a.decode_clusters);
+    const int splits =
+        choose_splits(n_tiles, nk, a.num_sms, a.decode_clusters ? a.decode_clusters + 2 * 9 : nullptr);
     // as in gemm_decode.cu: a grid of at most two CTAs per SM gets the
     // two-per-SM budget (deeper ring)
     const bool two = static_cast<int64_t>(n_tiles) * splits <= 2 * a.num_sms;

@@ -362,9 +362,10 @@ __global__ void __launch_bounds__(kThreads) decode_residency_probe() {}
 
 }  // namespace
 
-int gemm_decode_resident_clusters(int size) {
+int gemm_decode_resident_clusters(int size, int ctas_per_sm) {
+    const uint32_t smem = ctas_per_sm >= 3 ? kCtaSmem : ctas_per_sm == 2 ? kCtaSmem2 : kCtaSmem1;
     if (cudaFuncSetAttribute(decode_residency_probe, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kCtaSmem)) != cudaSuccess ||
+                             static_cast<int>(smem)) != cudaSuccess ||
         cudaFuncSetAttribute(decode_residency_probe,
                              cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
@@ -375,7 +376,7 @@ int gemm_decode_resident_clusters(int size) {
     cudaLaunchAttribute attr[1];
     cfg.gridDim = dim3(size, 1);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kCtaSmem;
+    cfg.dynamicSmemBytes = smem;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = size;
     attr[0].val.clusterDim.y = 1;
@@ -414,7 +415,8 @@ cudaError_t prepare_gemm_decode() {
 
 cudaError_t launch_gemm_decode(const GemmArgs& a) {
     const int n_tiles = (a.N + BNW - 1) / BNW;
-    const int splits = choose_splits(n_tiles, (a.K + BK - 1) / BK, a.num_sms, a.decode_clusters);
+    const int* clusters3 = a.decode_clusters ? a.decode_clusters + 2 * 9 : nullptr;
+    const int splits = choose_splits(n_tiles, (a.K + BK - 1) / BK, a.num_sms, clusters3);
     // A grid of at most two CTAs per SM gets the two-per-SM budget: a 4-5
     // stage ring instead of 3 (measured on the 8B decode step, 3852 -> 3923
     // GB/s; limiting it to token tiles of up to 16 was slower).  Partials are
@@ -428,12 +430,15 @@ cudaError_t launch_gemm_decode(const GemmArgs& a) {
     if (a.M <= 64) return launch_mt<64, false>(a, splits, budget);
     // Wider token tiles: a 32 KB (128 tokens) or 48 KB (256) ring stage and a
     // 64 / 128 KB partial, so two CTAs or one share an SM; the split is
-    // chosen for that many CTA slots.
+    // chosen for that footprint by the fewest-waves rule.
     const int nk = (a.K + BK - 1) / BK;
+    const int* clusters2 = a.decode_clusters ? a.decode_clusters + 1 * 9 : nullptr;
+    const int* clusters1 = a.decode_clusters;
     if (a.M <= 128)
-        return launch_mt<128, false>(a, choose_splits(n_tiles, nk, a.num_sms, nullptr, 2),
-                                     kCtaSmem2);
-    return launch_mt<256, false>(a, choose_splits(n_tiles, nk, a.num_sms, nullptr, 1), kCtaSmem1);
+        return launch_mt<128, false>(
+            a, choose_splits_min_waves(n_tiles, nk, 2 * a.num_sms, clusters2), kCtaSmem2);
+    return launch_mt<256, false>(
+        a, choose_splits_min_waves(n_tiles, nk, a.num_sms, clusters1), kCtaSmem1);
 }
 
 }  // namespace fp8k

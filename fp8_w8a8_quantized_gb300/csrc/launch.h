@@ -34,8 +34,9 @@ struct GemmArgs {
     int num_sms;
     bool pdl;             // launch as a programmatic dependent of the previous kernel
     int pair_clusters;    // co-resident clusters of the paired-SM kernel (0: unknown)
-    // decode_clusters[S]: clusters of S decode-GEMM CTAs that can be resident
-    // at once (index 1..8; null or 0: unknown)
+    // decode_clusters[(c - 1) * 9 + S]: clusters of S decode-GEMM CTAs that
+    // can be resident at once with the footprint of c CTAs per SM (c = 1..3,
+    // S = 1..8; null or 0: unknown)
     const int* decode_clusters = nullptr;
     cudaStream_t stream;
 };
@@ -59,7 +60,7 @@ int gemm_pair_resident_clusters(int num_sms);
 cudaError_t launch_gemm_decode(const GemmArgs& a);
 // How many clusters of `size` decode-GEMM CTAs can be resident at once (a
 // cluster must fit on the SMs of one GPC); 0 if unknown.
-int gemm_decode_resident_clusters(int size);
+int gemm_decode_resident_clusters(int size, int ctas_per_sm);
 
 // Quantization with other scale granularities (quant_variants.cu).
 // Every row quantized with the scale *s; s_rows (optional) gets s per row.

@@ -72,6 +72,29 @@ int main() {
     // 224 slabs of 4096 -> 28672 -> 2
     CHECK(choose_splits(32, 32, 152, clusters) == 8, "O-proj split");
     CHECK(choose_splits(224, 32, 152, clusters) == 2, "gate/up split");
+    // wide token tiles: the fewest waves, then the largest split (brute force)
+    for (int n_tiles = 1; n_tiles <= 400; n_tiles += 3)
+        for (int nk = 1; nk <= 120; nk += 5)
+            for (int slots : {152, 304})
+                for (const int* cl : {static_cast<const int*>(nullptr), clusters}) {
+                    const int S = choose_splits_min_waves(n_tiles, nk, slots, cl);
+                    auto waves = [&](int s) {
+                        const int pw = (cl && cl[s] > 0) ? cl[s] : slots / s;
+                        return (n_tiles + pw - 1) / pw;
+                    };
+                    CHECK(S >= 1 && S <= kMaxSplits && (S == 1 || nk >= 2 * S),
+                          "wide tiles=%d nk=%d S=%d", n_tiles, nk, S);
+                    for (int s = 1; s <= kMaxSplits && (s == 1 || nk >= 2 * s); ++s) {
+                        CHECK(waves(s) >= waves(S), "wide tiles=%d nk=%d: S=%d not fewest", n_tiles,
+                              nk, S);
+                        CHECK(!(waves(s) == waves(S) && s > S), "wide tiles=%d nk=%d: S=%d not largest",
+                              n_tiles, nk, S);
+                    }
+                }
+    // 224 slabs on 304 slots fit one wave unsplit; 48 slabs take the largest
+    // split that still fits one wave
+    CHECK(choose_splits_min_waves(224, 32, 304, nullptr) == 1, "wide gate/up");
+    CHECK(choose_splits_min_waves(48, 32, 304, nullptr) == 6, "wide QKV");
     std::printf(fails ? "FAIL %d\n" : "OK\n", fails);
     return fails ? 1 : 0;
 }
