@@ -83,6 +83,22 @@ inline int choose_splits(int n_tiles, int nk, int num_sms, const int* clusters =
     return best;
 }
 
+// Split count for the 32- and 64-token tiles, whose partials are pulled
+// across the cluster after a barrier (the tail grows with S and waits for
+// the slowest CTA): about kPullTargetCtas CTAs per layer, S = the nearest
+// integer to kPullTargetCtas / n_tiles, lowered until every cluster of S is
+// resident at once (clusters[S] when known) and each split has at least 2
+// k-blocks.  Against the busy-slot rule: 70B decode layers at 32 tokens
+// +3.1% (S = 3 / 4 / 1 / 4 instead of 5 / 6 / 1 / 6), the 8B decode step
+// unchanged; targets of 192 and 224 CTAs were slower on the 8B step.
+constexpr int kPullTargetCtas = 256;
+inline int choose_splits_pull(int n_tiles, int nk, const int* clusters) {
+    int s = (kPullTargetCtas + n_tiles / 2) / n_tiles;
+    s = s < 1 ? 1 : (s > kMaxSplits ? kMaxSplits : s);
+    while (s > 1 && (nk < 2 * s || (clusters && clusters[s] > 0 && clusters[s] < n_tiles))) --s;
+    return s;
+}
+
 // Split count for the wide token tiles (128 and 256 tokens: two CTAs or one
 // per SM, slots = ctas_per_sm x num_sms), whose per-CTA overhead (ring fill,
 // a 64-128 KB partial pulled across the cluster) makes every extra wave

@@ -416,7 +416,11 @@ cudaError_t prepare_gemm_decode() {
 cudaError_t launch_gemm_decode(const GemmArgs& a) {
     const int n_tiles = (a.N + BNW - 1) / BNW;
     const int* clusters3 = a.decode_clusters ? a.decode_clusters + 2 * 9 : nullptr;
-    const int splits = choose_splits(n_tiles, (a.K + BK - 1) / BK, a.num_sms, clusters3);
+    const int nk = (a.K + BK - 1) / BK;
+    // pushed partials (up to 16 tokens): the busy-slot rule; pulled: the
+    // target-CTA rule
+    const int splits = a.M <= 16 ? choose_splits(n_tiles, nk, a.num_sms, clusters3)
+                                 : choose_splits_pull(n_tiles, nk, clusters3);
     // A grid of at most two CTAs per SM gets the two-per-SM budget: a 4-5
     // stage ring instead of 3 (measured on the 8B decode step, 3852 -> 3923
     // GB/s; limiting it to token tiles of up to 16 was slower).  Partials are
@@ -431,7 +435,6 @@ cudaError_t launch_gemm_decode(const GemmArgs& a) {
     // Wider token tiles: a 32 KB (128 tokens) or 48 KB (256) ring stage and a
     // 64 / 128 KB partial, so two CTAs or one share an SM; the split is
     // chosen for that footprint by the fewest-waves rule.
-    const int nk = (a.K + BK - 1) / BK;
     const int* clusters2 = a.decode_clusters ? a.decode_clusters + 1 * 9 : nullptr;
     const int* clusters1 = a.decode_clusters;
     if (a.M <= 128)

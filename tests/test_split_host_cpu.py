@@ -91,6 +91,19 @@ int main() {
                               n_tiles, nk, S);
                     }
                 }
+    // pulled tiles: about 256 CTAs, every cluster resident, >= 2 k-blocks
+    for (int n_tiles = 1; n_tiles <= 512; ++n_tiles)
+        for (int nk = 1; nk <= 240; nk += 7) {
+            const int S = choose_splits_pull(n_tiles, nk, clusters);
+            CHECK(S >= 1 && S <= kMaxSplits && (S == 1 || nk >= 2 * S),
+                  "pull tiles=%d nk=%d S=%d", n_tiles, nk, S);
+            CHECK(S == 1 || clusters[S] >= n_tiles, "pull tiles=%d S=%d not resident", n_tiles, S);
+        }
+    CHECK(choose_splits_pull(80, 64, clusters) == 3, "70B QKV at 32 tokens");
+    CHECK(choose_splits_pull(64, 64, clusters) == 4, "70B O at 32 tokens");
+    CHECK(choose_splits_pull(64, 224, clusters) == 4, "70B down at 32 tokens");
+    CHECK(choose_splits_pull(448, 64, clusters) == 1, "70B gate/up at 32 tokens");
+    CHECK(choose_splits_pull(48, 32, clusters) == 5, "8B QKV at 32 tokens");
     // 224 slabs on 304 slots fit one wave unsplit; 48 slabs take the largest
     // split that still fits one wave
     CHECK(choose_splits_min_waves(224, 32, 304, nullptr) == 1, "wide gate/up");
