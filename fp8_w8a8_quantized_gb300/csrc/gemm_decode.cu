@@ -96,8 +96,29 @@ Layout layout_of(int M, int splits, int64_t budget) {
     return l;
 }
 
+// Barrier of the four epilogue warps (named barrier 1, 128 threads).
+__device__ __forceinline__ void epi_bar_sync() {
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// y[m, n] = bf16((v[j] * s_tok[m]) * s_w_n) for tokens m = m0 + j < M, one
+// weight row n per lane (a warp stores 32 consecutive outputs of a token).
+template <int NV>
+__device__ __forceinline__ void store_rows_direct(const float (&v)[NV], int m0, int M, int N,
+                                                  int n, const float* s_tok, float s_w_n,
+                                                  __nv_bfloat16* __restrict__ y) {
+    if (n >= N) return;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        const int m = m0 + j;
+        if (m < M)
+            y[static_cast<int64_t>(m) * N + n] = __float2bfloat16_rn((v[j] * s_tok[m]) * s_w_n);
+    }
+}
+
 // PUSH: partials pushed into a dedicated receive buffer (no cluster barrier
-// after the main loop); otherwise pulled from the idle ring.
+// after the main loop); otherwise pulled from the idle ring, or, unsplit
+// (S = 1), stored by each CTA straight from its accumulator.
 template <int MT, bool PUSH>
 __global__ void __launch_bounds__(kThreads)
     gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW,
@@ -261,6 +282,12 @@ __global__ void __launch_bounds__(kThreads)
                 // owner's barrier completes.
                 cluster_wait();
                 push_send<MT>(v, M, nl, rank, splits, recv, &bars->recv_full);
+            } else if (splits == 1) {
+                // Unsplit: this CTA owns the whole slab; scale and store
+                // straight from registers (no ring copy, no cluster barrier).
+                epi_bar_sync();  // the scales staged by warps 2 and 3
+                store_rows_direct<MT>(v, 0, M, N, n_blk * BNW + nl, bars->s_tok,
+                                      bars->s_w[nl], y);
             } else {
                 // The ring is idle once the accumulator is complete (every
                 // stage was consumed by an MMA that has finished): reuse it.
@@ -273,6 +300,7 @@ __global__ void __launch_bounds__(kThreads)
             // (a wide tile's accumulator row would not fit in registers).
             if (nkb > 0) have = warp_wait(&bars->acc_full, 0, abort_flag, status);
             if (have) tc_fence_after();
+            if (splits == 1) epi_bar_sync();  // the scales staged by warps 2 and 3
 #pragma unroll 1
             for (int h = 0; h < MT / 32; ++h) {
                 uint32_t r[32];
@@ -280,9 +308,18 @@ __global__ void __launch_bounds__(kThreads)
                     tmem_ld_32x32b_x32(tacc + h * 32, r);
                     tmem_ld_wait();
                 }
+                if (splits == 1) {
+                    // unsplit: scale and store straight from registers
+                    float v[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    red[(h * 32 + j) * BNW + nl] = have ? __uint_as_float(r[j]) : 0.0f;
+                    for (int j = 0; j < 32; ++j) v[j] = have ? __uint_as_float(r[j]) : 0.0f;
+                    store_rows_direct<32>(v, h * 32, M, N, n_blk * BNW + nl, bars->s_tok,
+                                          bars->s_w[nl], y);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        red[(h * 32 + j) * BNW + nl] = have ? __uint_as_float(r[j]) : 0.0f;
+                }
             }
             tc_fence_before();
         }
@@ -310,6 +347,14 @@ __global__ void __launch_bounds__(kThreads)
             push_reduce(recv, splits, lo, width, M, store);
         else
             outlive_peers();
+    } else if (splits == 1) {
+        // unsplit: the epilogue warps have stored the outputs; every tcgen05
+        // operation has completed once all warps are here
+        __syncthreads();
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(tmem_base, C::TMEM_COLS);
+        }
     } else {
         // All partials of the cluster are in shared memory after this
         // barrier, and every tcgen05 operation of this CTA has completed.
@@ -331,7 +376,8 @@ cudaError_t launch_mt(const GemmArgs& a, int splits, uint32_t budget) {
     if (!encode_tmap_u8(&tmX, a.xq, a.M, a.K, a.K, BK, MT)) return cudaErrorInvalidValue;
     const int n_tiles = (a.N + BNW - 1) / BNW;
     const Layout l = layout_of<MT, PUSH>(a.M, splits, budget);
-    if (l.stages < 2 || (!PUSH && Cfg<MT>::RED_BYTES > l.stages * Cfg<MT>::STAGE_BYTES))
+    if (l.stages < 2 ||
+        (!PUSH && splits > 1 && Cfg<MT>::RED_BYTES > l.stages * Cfg<MT>::STAGE_BYTES))
         return cudaErrorInvalidConfiguration;
 
     cudaLaunchConfig_t cfg = {};
@@ -440,8 +486,10 @@ cudaError_t launch_gemm_decode(const GemmArgs& a) {
     if (a.M <= 128)
         return launch_mt<128, false>(
             a, choose_splits_min_waves(n_tiles, nk, 2 * a.num_sms, clusters2), kCtaSmem2);
-    return launch_mt<256, false>(
-        a, choose_splits_min_waves(n_tiles, nk, a.num_sms, clusters1), kCtaSmem1);
+    // Unsplit, a 256-token tile needs no ring room for a partial: two CTAs
+    // (two 48 KB stages each) then share an SM.
+    const int s256 = choose_splits_min_waves(n_tiles, nk, a.num_sms, clusters1);
+    return launch_mt<256, false>(a, s256, s256 == 1 ? kCtaSmem2 : kCtaSmem1);
 }
 
 }  // namespace fp8k
