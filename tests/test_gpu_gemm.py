@@ -59,6 +59,7 @@ MULTI_TILE = [
     (200, 28672, 1024),   # 256-token tiles, 224 slabs
     (255, 49152, 256),    # 256-token tiles, 384 slabs, two k-blocks (no K split)
     (80, 24576, 512),     # 128-token tiles, 48 of 128 token columns empty
+    (8, 57344, 1024),     # 448 slabs, unsplit, 16-token tiles (pushed to themselves)
     (1024, 8192, 1024),   # paired: 4 x 32 = 128 tiles, up to 2 per pair
     (1536, 8192, 256),    # paired: 6 x 32 = 192 tiles, up to 3 per pair
     (2304, 4864, 272),    # paired: 9 x 19 = 171 tiles, ragged K
