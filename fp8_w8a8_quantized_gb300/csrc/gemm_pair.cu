@@ -258,9 +258,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1],
                                                 packed[4 * j + 2], packed[4 * j + 3]);
                     } else {
+                        // unrolled with a guard per column: a loop bound on
+                        // N would index packed[] at run time and put it in
+                        // local memory for every chunk
                         uint16_t* dst = reinterpret_cast<uint16_t*>(yrow + n0);
-                        for (int j = 0; j < 32 && n0 + j < N; ++j)
-                            dst[j] = static_cast<uint16_t>(packed[j >> 1] >> ((j & 1) * 16));
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (n0 + j < N)
+                                dst[j] = static_cast<uint16_t>(packed[j >> 1] >> ((j & 1) * 16));
                     }
                 }
             };

@@ -1,7 +1,7 @@
 """GPU parity of the scaled FP8 GEMM (both kernels: the weight-streaming
 split-K kernel for M <= 256, token tiles of 16 to 256, and the paired-SM
-256 x 256 tile kernel above, partial row tiles included), fed with the
-oracle's own codes and scales, against the oracle's fp64 result."""
+256 x 256 tile kernel above, partial row and column tiles included), fed
+with the oracle's own codes and scales, against the oracle's fp64 result."""
 import numpy as np
 import pytest
 import torch
@@ -53,7 +53,7 @@ def test_random_codes(oracle_mod, M, N, K):
 # The persistent paired-SM kernel walking more than one output tile per CTA
 # pair (at most 76 pairs of 256 x 256 tiles): the second TMEM accumulator
 # buffer, its phase flips and the tile walk; rows of a tile past M are
-# zero-filled by TMA and never stored.  And the weight-streaming kernel with
+# zero-filled by TMA and never stored, nor are columns past N.  And the weight-streaming kernel with
 # wide token tiles over many weight slabs.  Full outputs against the oracle.
 MULTI_TILE = [
     (200, 28672, 1024),   # 256-token tiles, 224 slabs
@@ -63,6 +63,9 @@ MULTI_TILE = [
     (1024, 8192, 1024),   # paired: 4 x 32 = 128 tiles, up to 2 per pair
     (1536, 8192, 256),    # paired: 6 x 32 = 192 tiles, up to 3 per pair
     (2304, 4864, 272),    # paired: 9 x 19 = 171 tiles, ragged K
+    (2048, 16384, 272),   # paired: 8 x 64 = 512 tiles, up to 7 per pair, ragged K
+    (1800, 12296, 144),   # paired: 8 rows in the last row tile, 8 columns in the last
+    (1032, 20812, 256),   # paired: 5 x 82 tiles, last column tile 76 wide (not 8-aligned)
 ]
 
 
