@@ -44,6 +44,9 @@ class Fp8Error(RuntimeError):
 def lib() -> ctypes.CDLL:
     """The loaded CUDA library, with argument types declared."""
     global _lib
+    L = _lib
+    if L is not None:  # loaded: no lock on the per-call path
+        return L
     with _lock:
         if _lib is not None:
             return _lib
@@ -189,9 +192,8 @@ def fp8_linear(x: torch.Tensor, wq: torch.Tensor, s_w: torch.Tensor,
     N = wq.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
-    need = fp8_linear_workspace_size(M, N, K)
-    if workspace is None:
-        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=x.device)
+    if workspace is None:  # (a given workspace is size-checked by the library)
+        workspace = torch.empty((max(fp8_linear_workspace_size(M, N, K), 1),), dtype=torch.uint8, device=x.device)
     _check(lib().fp8_linear(_ptr(x), _ptr(wq), _ptr(s_w), _ptr(y), M, N, K,
                             _ptr(workspace), workspace.numel(), _stream(stream)), "fp8_linear")
     return y
@@ -301,9 +303,8 @@ def fp8_linear_rmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float, wq: tor
     N = wq.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
-    need = fp8_linear_workspace_size(M, N, K)
-    if workspace is None:
-        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=x.device)
+    if workspace is None:  # (a given workspace is size-checked by the library)
+        workspace = torch.empty((max(fp8_linear_workspace_size(M, N, K), 1),), dtype=torch.uint8, device=x.device)
     _check(lib().fp8_linear_rmsnorm(_ptr(x), _ptr(gamma), float(eps), _ptr(wq), _ptr(s_w),
                                     _ptr(y), M, N, K, _ptr(workspace), workspace.numel(),
                                     _stream(stream)), "fp8_linear_rmsnorm")
@@ -371,9 +372,8 @@ def fp8_linear_blockwise(x: torch.Tensor, wq: torch.Tensor, s_w: torch.Tensor,
     N = wq.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
-    need = fp8_linear_blockwise_workspace_size(M, N, K)
-    if workspace is None:
-        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=x.device)
+    if workspace is None:  # (a given workspace is size-checked by the library)
+        workspace = torch.empty((max(fp8_linear_blockwise_workspace_size(M, N, K), 1),), dtype=torch.uint8, device=x.device)
     _check(lib().fp8_linear_blockwise(_ptr(x), _ptr(wq), _ptr(s_w), _ptr(y), M, N, K,
                                       _ptr(workspace), workspace.numel(), _stream(stream)),
            "fp8_linear_blockwise")
