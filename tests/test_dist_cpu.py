@@ -66,3 +66,22 @@ def test_reference_arm_prints_once_under_torchrun():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_clock_record_parsing():
+    """The clocks record the bench prints beside every number: median SM
+    clock and power over the samples taken during the timed region, and the
+    throttle reasons seen active in any of them (nvidia-smi csv, no units)."""
+    import bench
+    c = bench.ClockSampler(0)
+    c.lines = [
+        "0, 2070, 2070, 812.50, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "0, 1980, 2070, 1201.50, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 2070, 2070, 1000.00, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "garbage line",
+    ]
+    s = c.summary()
+    assert s == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "power_w": 1000.0,
+                 "reasons": ["sw_power_cap"], "samples": 3}
+    c.lines = []
+    assert bench.ClockSampler.summary(c)["sm_mhz"] is None
