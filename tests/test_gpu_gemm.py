@@ -39,6 +39,8 @@ SHAPES = [  # (M, N, K): ragged edges, single k-block, many k-blocks, both kerne
     (33, 1000, 4096), (64, 384, 2048), (65, 256, 256), (128, 256, 128), (129, 520, 1040),
     (200, 300, 4112), (256, 512, 4096), (300, 1000, 1024), (513, 777, 2064),
     (256, 256, 128), (257, 264, 256), (1000, 4100, 512), (2048, 520, 272), (384, 128, 8192),
+    # degenerate edges: one output column, the smallest K, one partial k-block
+    (5, 1, 32), (200, 3, 128), (300, 1, 64), (300, 520, 16), (512, 768, 48), (200, 300, 16),
 ]
 
 
