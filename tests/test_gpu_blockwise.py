@@ -106,7 +106,8 @@ def make_layer(M, N, K, seed, prefill=False):
 
 
 @pytest.mark.parametrize("M", [1, 8, 16, 17, 32, 48, 64])
-@pytest.mark.parametrize("N,K", [(1024, 4096), (4096, 1024), (300, 1040), (640, 14336)])
+@pytest.mark.parametrize("N,K", [(1024, 4096), (4096, 1024), (300, 1040), (640, 14336),
+                                 (1, 32), (3, 16)])
 def test_gemm_decode_sizes(oracle_mod, M, N, K):
     _, xq, s_x, wq, s_w = make_layer(M, N, K, 50 + M)
     y = pkg.fp8_scaled_gemm_blockwise(xq, s_x, wq, s_w)
@@ -118,7 +119,9 @@ def test_gemm_decode_sizes(oracle_mod, M, N, K):
 @pytest.mark.parametrize("M,N,K", [(65, 512, 1024), (130, 300, 1040), (256, 1024, 4096),
                                    (1000, 768, 2048), (129, 4096, 512),
                                    # 240 and 336 tiles on 152 persistent CTAs
-                                   (640, 12288, 512), (200, 43008, 256)])
+                                   (640, 12288, 512), (200, 43008, 256),
+                                   # one output column, K = 16, a partial k-block
+                                   (130, 1, 16), (300, 3, 144)])
 def test_gemm_prefill_sizes(oracle_mod, M, N, K):
     _, xq, s_x, wq, s_w = make_layer(M, N, K, 70 + M, prefill=True)
     y = pkg.fp8_scaled_gemm_blockwise(xq, s_x, wq, s_w)
