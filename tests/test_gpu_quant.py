@@ -56,7 +56,9 @@ def test_weight_channels(oracle_mod, N, K):
 
 
 @pytest.mark.parametrize("M,K", [(1, 16), (3, 48), (5, 272), (33, 1040), (7, 2064),
-                                 (130, 4112), (2, 65536), (3, 65552), (1, 131072)])
+                                 (130, 4112), (2, 65536), (3, 65552), (1, 131072),
+                                 # ragged rows in the many-rows layout (two chunks a thread)
+                                 (1000, 4112), (1300, 2064)])
 def test_ragged_and_long_rows(oracle_mod, M, K):
     g = torch.Generator(device=DEV)
     g.manual_seed(M * 7 + K)

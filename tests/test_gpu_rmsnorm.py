@@ -48,7 +48,7 @@ def check(oracle_mod, x, g, eps):
 
 @pytest.mark.parametrize("M,K", [(1, 4096), (8, 4096), (32, 14336), (2048, 4096), (8192, 4096),
                                  (3, 16), (5, 272), (33, 1040), (130, 4112), (3, 65536),
-                                 (2, 28672)])
+                                 (2, 28672), (1000, 4112), (1300, 2064)])
 def test_rmsnorm_quant(oracle_mod, M, K):
     x = workloads.student_t_outliers(M, K, workloads.SEED_PREFILL, DEV)
     amb = check(oracle_mod, x, gamma(K, K), 1e-6)

@@ -32,7 +32,7 @@ def randn(shape, seed, scale=3.0):
 # ---------------------------------------------------------------- static scale
 
 @pytest.mark.parametrize("M,K", [(1, 4096), (16, 4096), (32, 14336), (2048, 4096),
-                                 (3, 48), (7, 2064), (130, 4112)])
+                                 (3, 48), (7, 2064), (130, 4112), (1, 16), (1000, 4112)])
 @pytest.mark.parametrize("s_val", [1.0, 0.0123, 120.0 / 448.0])
 def test_static_scale(oracle_mod, M, K, s_val):
     x = workloads.gaussian_outliers(M, K, workloads.SEED_DECODE, DEV)
