@@ -12,7 +12,8 @@ than twice the L2 cache, so every step streams its weights from HBM.
 
 Printed (rank 0, one JSON line): value (device-timed, inputs resident),
 e2e (same metric through the public API with pinned host inputs/outputs
-copied in the timed region), roofline of the dominant kernel (the decode
+copied in the timed region; the step's calls replayed as a CUDA graph, and
+issued one by one from Python in e2e.eager), roofline of the dominant kernel (the decode
 GEMM), prefill TFLOPS of the 8B prefill shapes as context, the CPU oracle
 timed on a bounded sample, and the SM clocks seen during the timed region.
 
