@@ -125,6 +125,27 @@ def _ptr(t) -> int:
     return 0 if t is None else t.data_ptr()
 
 
+def _expect(t, name: str, shape: tuple, dtype, contiguous: bool = True):
+    """The kernels index raw device memory by the sizes they are given: every
+    tensor must be a CUDA tensor of exactly the expected shape and dtype (and
+    contiguous, or with unit stride along its last dimension)."""
+    if (not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_cuda
+            or tuple(t.shape) != tuple(shape)
+            or (not t.is_contiguous() if contiguous else (t.dim() == 2 and t.shape[1] > 1
+                                                          and t.stride(1) != 1))):
+        got = (f"{t.dtype} {tuple(t.shape)} on {t.device}"
+               f"{'' if t.is_contiguous() else ', not contiguous'}"
+               if isinstance(t, torch.Tensor) else type(t).__name__)
+        raise ValueError(f"{name} must be a CUDA {dtype} tensor of shape {tuple(shape)}"
+                         f"{', contiguous' if contiguous else ''}; got {got}")
+
+
+def _workspace(t, name: str = "workspace"):
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.uint8 or not t.is_cuda \
+            or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA uint8 tensor")
+
+
 def _rows(t: torch.Tensor, name: str):
     if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
         raise ValueError(f"{name} must be 2-D with unit stride along K")
@@ -148,10 +169,13 @@ def fp8_quant_per_token(x: torch.Tensor, xq: torch.Tensor | None = None,
                         s_tok: torch.Tensor | None = None, stream=None):
     """bf16 [M, K] -> (E4M3 codes uint8 [M, K], fp32 scales [M])."""
     M, K, ldx = _rows(x, "x")
+    _expect(x, "x", (M, K), torch.bfloat16, contiguous=False)
     if xq is None:
         xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
     if s_tok is None:
         s_tok = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _expect(xq, "xq", (M, K), torch.uint8, contiguous=False)
+    _expect(s_tok, "s_tok", (M,), torch.float32)
     _check(lib().fp8_quant_per_token(_ptr(x), M, K, ldx, _ptr(xq), xq.stride(0) if M else K,
                                      _ptr(s_tok), _stream(stream)), "fp8_quant_per_token")
     return xq, s_tok
@@ -161,10 +185,13 @@ def fp8_quant_per_channel_weights(w: torch.Tensor, wq: torch.Tensor | None = Non
                                   s_w: torch.Tensor | None = None, stream=None):
     """bf16 [N, K] -> (E4M3 codes uint8 [N, K], fp32 per-row scales [N])."""
     N, K, ldw = _rows(w, "w")
+    _expect(w, "w", (N, K), torch.bfloat16, contiguous=False)
     if wq is None:
         wq = torch.empty((N, K), dtype=torch.uint8, device=w.device)
     if s_w is None:
         s_w = torch.empty((N,), dtype=torch.float32, device=w.device)
+    _expect(wq, "wq", (N, K), torch.uint8, contiguous=False)
+    _expect(s_w, "s_w", (N,), torch.float32)
     _check(lib().fp8_quant_per_channel_weights(_ptr(w), N, K, ldw, _ptr(wq),
                                                wq.stride(0) if N else K, _ptr(s_w),
                                                _stream(stream)),
@@ -177,8 +204,13 @@ def fp8_scaled_gemm(xq: torch.Tensor, s_tok: torch.Tensor, wq: torch.Tensor,
     """(codes [M, K], scales [M]) x (codes [N, K], scales [N]) -> bf16 [M, N]."""
     M, K = xq.shape
     N = wq.shape[0]
+    _expect(xq, "xq", (M, K), torch.uint8)
+    _expect(s_tok, "s_tok", (M,), torch.float32)
+    _expect(wq, "wq", (N, K), torch.uint8)
+    _expect(s_w, "s_w", (N,), torch.float32)
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    _expect(y, "y", (M, N), torch.bfloat16)
     _check(lib().fp8_scaled_gemm(_ptr(xq), _ptr(s_tok), _ptr(wq), _ptr(s_w), _ptr(y),
                                  M, N, K, None, 0, _stream(stream)), "fp8_scaled_gemm")
     return y
@@ -190,10 +222,15 @@ def fp8_linear(x: torch.Tensor, wq: torch.Tensor, s_w: torch.Tensor,
     """The whole W8A8 layer: bf16 X [M, K] and offline-quantized W -> bf16 [M, N]."""
     M, K = x.shape
     N = wq.shape[0]
+    _expect(x, "x", (M, K), torch.bfloat16)
+    _expect(wq, "wq", (N, K), torch.uint8)
+    _expect(s_w, "s_w", (N,), torch.float32)
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _expect(y, "y", (M, N), torch.bfloat16)
     if workspace is None:  # (a given workspace is size-checked by the library)
         workspace = torch.empty((max(fp8_linear_workspace_size(M, N, K), 1),), dtype=torch.uint8, device=x.device)
+    _workspace(workspace)
     _check(lib().fp8_linear(_ptr(x), _ptr(wq), _ptr(s_w), _ptr(y), M, N, K,
                             _ptr(workspace), workspace.numel(), _stream(stream)), "fp8_linear")
     return y
@@ -301,10 +338,16 @@ def fp8_linear_rmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float, wq: tor
     per-token quantization fused into the normalisation kernel."""
     M, K = x.shape
     N = wq.shape[0]
+    _expect(x, "x", (M, K), torch.bfloat16)
+    _expect(gamma, "gamma", (K,), torch.bfloat16)
+    _expect(wq, "wq", (N, K), torch.uint8)
+    _expect(s_w, "s_w", (N,), torch.float32)
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _expect(y, "y", (M, N), torch.bfloat16)
     if workspace is None:  # (a given workspace is size-checked by the library)
         workspace = torch.empty((max(fp8_linear_workspace_size(M, N, K), 1),), dtype=torch.uint8, device=x.device)
+    _workspace(workspace)
     _check(lib().fp8_linear_rmsnorm(_ptr(x), _ptr(gamma), float(eps), _ptr(wq), _ptr(s_w),
                                     _ptr(y), M, N, K, _ptr(workspace), workspace.numel(),
                                     _stream(stream)), "fp8_linear_rmsnorm")
@@ -352,8 +395,13 @@ def fp8_scaled_gemm_blockwise(xq: torch.Tensor, s_x: torch.Tensor, wq: torch.Ten
     """Block-scaled GEMM: (codes [M, K], s_x [M, KB]) x (codes [N, K], s_w [NB, KB]) -> bf16."""
     M, K = xq.shape
     N = wq.shape[0]
+    _expect(xq, "xq", (M, K), torch.uint8)
+    _expect(s_x, "s_x", (M, _blocks(K)), torch.float32)
+    _expect(wq, "wq", (N, K), torch.uint8)
+    _expect(s_w, "s_w", (_blocks(N), _blocks(K)), torch.float32)
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    _expect(y, "y", (M, N), torch.bfloat16)
     _check(lib().fp8_scaled_gemm_blockwise(_ptr(xq), _ptr(s_x), _ptr(wq), _ptr(s_w), _ptr(y),
                                            M, N, K, None, 0, _stream(stream)),
            "fp8_scaled_gemm_blockwise")
@@ -370,10 +418,15 @@ def fp8_linear_blockwise(x: torch.Tensor, wq: torch.Tensor, s_w: torch.Tensor,
     """The block-scaled layer: bf16 X [M, K] and block-quantized W -> bf16 [M, N]."""
     M, K = x.shape
     N = wq.shape[0]
+    _expect(x, "x", (M, K), torch.bfloat16)
+    _expect(wq, "wq", (N, K), torch.uint8)
+    _expect(s_w, "s_w", (_blocks(N), _blocks(K)), torch.float32)
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _expect(y, "y", (M, N), torch.bfloat16)
     if workspace is None:  # (a given workspace is size-checked by the library)
         workspace = torch.empty((max(fp8_linear_blockwise_workspace_size(M, N, K), 1),), dtype=torch.uint8, device=x.device)
+    _workspace(workspace)
     _check(lib().fp8_linear_blockwise(_ptr(x), _ptr(wq), _ptr(s_w), _ptr(y), M, N, K,
                                       _ptr(workspace), workspace.numel(), _stream(stream)),
            "fp8_linear_blockwise")

@@ -212,3 +212,37 @@ def test_calls_that_pass_the_checks_report_a_cuda_error_without_a_device(L):
     assert L.fp8_linear(fake, fake, fake, fake, 4, 4, 32, fake, 4096, None) == CUDA
     assert L.fp8_device_status(0) == CUDA
     assert L.fp8_selftest_wait_timeout(1_000_000, fake, None) == CUDA
+
+
+def test_binding_rejects_tensors_the_kernels_cannot_take():
+    """The Python binding checks shape, dtype, device and layout of every
+    tensor before the C call, since the kernels index raw memory by the
+    sizes they are given (CPU tensors are rejected too: no call is made)."""
+    import torch
+    import fp8_w8a8_quantized_gb300 as pkg
+
+    M, K, N = 4, 64, 8
+    x = torch.zeros(M, K, dtype=torch.bfloat16)
+    wq = torch.zeros(N, K, dtype=torch.uint8)
+    s_w = torch.ones(N, dtype=torch.float32)
+    with pytest.raises(ValueError, match="x must be a CUDA"):
+        pkg.fp8_linear(x, wq, s_w)                         # host memory
+    with pytest.raises(ValueError, match="x must be a CUDA"):
+        pkg.fp8_quant_per_token(x)
+    with pytest.raises(ValueError, match="w must be a CUDA"):
+        pkg.fp8_quant_per_channel_weights(x)
+    with pytest.raises(ValueError, match="xq must be a CUDA"):
+        pkg.fp8_scaled_gemm(wq[:M], s_w[:M], wq, s_w)
+    with pytest.raises(ValueError, match="xq must be a CUDA"):
+        pkg.fp8_scaled_gemm_blockwise(wq[:M], s_w[:M], wq, s_w)
+    with pytest.raises(ValueError, match="x must be a CUDA"):
+        pkg.fp8_linear_blockwise(x, wq, s_w)
+    with pytest.raises(ValueError, match="x must be a CUDA"):
+        pkg.fp8_linear_rmsnorm(x, x[0], 1e-6, wq, s_w)
+    # the messages name what was wrong
+    with pytest.raises(ValueError, match=r"shape \(8,\), contiguous; got torch.float32 \(7,\)"):
+        pkg._binding._expect(s_w[:7], "s_w", (N,), torch.float32)
+    with pytest.raises(ValueError, match="not contiguous"):
+        pkg._binding._expect(x.t(), "y", (K, M), torch.bfloat16)
+    with pytest.raises(ValueError, match="uint8"):
+        pkg._binding._workspace(torch.zeros(4, dtype=torch.float32))
