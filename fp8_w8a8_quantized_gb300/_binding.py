@@ -241,8 +241,15 @@ def fp8_quant_static(x: torch.Tensor, s: torch.Tensor, xq: torch.Tensor | None =
     """bf16 [M, K] with a given fp32 scale s [1] -> E4M3 codes uint8 [M, K].
     If s_rows (fp32 [M]) is given, s is written to every entry."""
     M, K, ldx = _rows(x, "x")
+    _expect(x, "x", (M, K), torch.bfloat16, contiguous=False)
+    _expect(s, "s", tuple(s.shape), torch.float32)
+    if s.numel() != 1:
+        raise ValueError("s must hold one scale")
     if xq is None:
         xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    _expect(xq, "xq", (M, K), torch.uint8, contiguous=False)
+    if s_rows is not None:
+        _expect(s_rows, "s_rows", (M,), torch.float32)
     _check(lib().fp8_quant_static(_ptr(x), M, K, ldx, _ptr(s), _ptr(xq),
                                   xq.stride(0) if M else K, _ptr(s_rows), _stream(stream)),
            "fp8_quant_static")
@@ -255,13 +262,21 @@ def fp8_quant_per_tensor(x: torch.Tensor, xq: torch.Tensor | None = None,
     """bf16 [M, K] -> (E4M3 codes uint8 [M, K], fp32 scale [1]) with one
     dynamic scale amax / 448 for the whole tensor."""
     M, K, ldx = _rows(x, "x")
+    _expect(x, "x", (M, K), torch.bfloat16, contiguous=False)
     if xq is None:
         xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
     if s is None:
         s = torch.empty((1,), dtype=torch.float32, device=x.device)
+    _expect(xq, "xq", (M, K), torch.uint8, contiguous=False)
+    _expect(s, "s", tuple(s.shape), torch.float32)
+    if s.numel() != 1:
+        raise ValueError("s must hold one scale")
+    if s_rows is not None:
+        _expect(s_rows, "s_rows", (M,), torch.float32)
     need = int(lib().fp8_quant_per_tensor_workspace_size(M, K))
     if workspace is None:
         workspace = torch.empty((need,), dtype=torch.uint8, device=x.device)
+    _workspace(workspace)
     _check(lib().fp8_quant_per_tensor(_ptr(x), M, K, ldx, _ptr(xq), xq.stride(0) if M else K,
                                       _ptr(s), _ptr(s_rows), _ptr(workspace), workspace.numel(),
                                       _stream(stream)), "fp8_quant_per_tensor")
@@ -278,6 +293,11 @@ def fp8_kv_cache_quant(kv: torch.Tensor, scale: torch.Tensor, cache: torch.Tenso
     T, H, D = kv.shape
     if cache.shape[1:] != (H, D):
         raise ValueError("cache must be [n_slots, H, D]")
+    _expect(kv, "kv", (T, H, D), torch.bfloat16)
+    _expect(cache, "cache", tuple(cache.shape), torch.uint8)
+    _expect(scale, "scale", tuple(scale.shape), torch.float32)
+    if slot_mapping is not None:
+        _expect(slot_mapping, "slot_mapping", (T,), torch.int64)
     stride = 1 if scale.numel() == H and H > 1 else 0
     if stride == 0 and scale.numel() != 1:
         raise ValueError("scale must have 1 or H entries")
@@ -298,6 +318,14 @@ def fp8_kv_cache_quant_kv(k: torch.Tensor, v: torch.Tensor, k_scale: torch.Tenso
     T, H, D = k.shape
     if v.shape != k.shape or k_cache.shape != v_cache.shape or k_cache.shape[1:] != (H, D):
         raise ValueError("k and v must be [T, H, D], both caches [n_slots, H, D]")
+    for t, name in ((k, "k"), (v, "v")):
+        _expect(t, name, (T, H, D), torch.bfloat16)
+    for t, name in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _expect(t, name, tuple(k_cache.shape), torch.uint8)
+    for t, name in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _expect(t, name, tuple(t.shape), torch.float32)
+    if slot_mapping is not None:
+        _expect(slot_mapping, "slot_mapping", (T,), torch.int64)
     if k_scale.numel() != v_scale.numel():
         raise ValueError("k_scale and v_scale must have the same number of entries")
     stride = 1 if k_scale.numel() == H and H > 1 else 0
@@ -317,6 +345,8 @@ def fp8_rmsnorm_quant(x: torch.Tensor, gamma: torch.Tensor, eps: float,
     Returns (codes uint8 [M, K], fp32 scales [M], normalised bf16 rows or
     None); pass y=True (or a bf16 [M, K] tensor) to get the rows."""
     M, K, ldx = _rows(x, "x")
+    _expect(x, "x", (M, K), torch.bfloat16, contiguous=False)
+    _expect(gamma, "gamma", (K,), torch.bfloat16)
     if xq is None:
         xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
     if s_tok is None:
@@ -325,6 +355,10 @@ def fp8_rmsnorm_quant(x: torch.Tensor, gamma: torch.Tensor, eps: float,
         y = torch.empty((M, K), dtype=torch.bfloat16, device=x.device)
     elif y is False:
         y = None
+    _expect(xq, "xq", (M, K), torch.uint8, contiguous=False)
+    _expect(s_tok, "s_tok", (M,), torch.float32)
+    if y is not None:
+        _expect(y, "y", (M, K), torch.bfloat16)
     _check(lib().fp8_rmsnorm_quant(_ptr(x), _ptr(gamma), float(eps), M, K, ldx, _ptr(xq),
                                    xq.stride(0) if M else K, _ptr(s_tok), _ptr(y),
                                    _stream(stream)), "fp8_rmsnorm_quant")
@@ -366,10 +400,13 @@ def fp8_quant_per_token_group(x: torch.Tensor, xq: torch.Tensor | None = None,
     """bf16 [M, K] -> (codes uint8 [M, K], fp32 scales [M, ceil(K/128)]),
     one scale per token per 128 inputs."""
     M, K, ldx = _rows(x, "x")
+    _expect(x, "x", (M, K), torch.bfloat16, contiguous=False)
     if xq is None:
         xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
     if s_x is None:
         s_x = torch.empty((M, _blocks(K)), dtype=torch.float32, device=x.device)
+    _expect(xq, "xq", (M, K), torch.uint8, contiguous=False)
+    _expect(s_x, "s_x", (M, _blocks(K)), torch.float32)
     _check(lib().fp8_quant_per_token_group(_ptr(x), M, K, ldx, _ptr(xq), xq.stride(0) if M else K,
                                            _ptr(s_x), _stream(stream)),
            "fp8_quant_per_token_group")
@@ -381,10 +418,13 @@ def fp8_quant_weight_blocks(w: torch.Tensor, wq: torch.Tensor | None = None,
     """bf16 [N, K] -> (codes uint8 [N, K], fp32 scales [ceil(N/128), ceil(K/128)]),
     one scale per 128 x 128 block."""
     N, K, ldw = _rows(w, "w")
+    _expect(w, "w", (N, K), torch.bfloat16, contiguous=False)
     if wq is None:
         wq = torch.empty((N, K), dtype=torch.uint8, device=w.device)
     if s_w is None:
         s_w = torch.empty((_blocks(N), _blocks(K)), dtype=torch.float32, device=w.device)
+    _expect(wq, "wq", (N, K), torch.uint8, contiguous=False)
+    _expect(s_w, "s_w", (_blocks(N), _blocks(K)), torch.float32)
     _check(lib().fp8_quant_weight_blocks(_ptr(w), N, K, ldw, _ptr(wq), wq.stride(0) if N else K,
                                          _ptr(s_w), _stream(stream)), "fp8_quant_weight_blocks")
     return wq, s_w
