@@ -2,7 +2,10 @@
 
 Argument marshalling only: every step of the layer runs in the CUDA library
 (``_build/libfp8w8a8.so``).  If the library is missing the calls raise; there
-is no CPU or PyTorch fallback.
+is no CPU or PyTorch fallback.  Since the C ABI takes raw pointers and sizes,
+each call first checks that its tensors are CUDA tensors of the shapes and
+dtypes the sizes imply (ValueError otherwise); the library checks the rest
+(alignment, K % 16, workspace size) and its status becomes Fp8Error.
 """
 from __future__ import annotations
 
